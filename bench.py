@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE FFN layer forward on GB300: tokens/s and fraction of roofline.
+
+Default workload: the 350M+MoE-128 layer (d=1024, f=4096, E=128 experts, top-1, capacity
+factor 1.25) at T = 4096 tokens, fp16 weights and activations with fp32 accumulation, all
+expert weights (2.15 GB) resident in HBM.  A step is one moe_layer_forward call (gate,
+dispatch, both expert GEMMs with fused GeLU and combine) on one of 4 seeded token batches,
+cycled so routing changes from step to step; the expert weights alone exceed L2 (129 MB)
+several times over, so every step streams them from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (under torchrun): independent replicas, one per GPU (weak scaling); each rank times
+its K steps between barriers, the slowest rank's time counts.  --impl reference times the
+plain CPU oracle on the host cores on sub-batches of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/sec on 1 GB300 and % of roofline (tensor peak or HBM GB/s)"
+UNIT = "tokens/s"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="moe350m_e128")
+    p.add_argument("--tokens", type=int, default=4096)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget-s", type=float, default=20.0)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------------ clocks sampler
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [s for t, s in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not inside:
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[1]]
+        sm = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4)
+                          if len(s) > 5 + i and s[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------------------ CPU oracle timing
+class OracleRunner:
+    """The plain CPU oracle on contiguous sub-batches of the workload: each sub-batch is a full
+    layer call of its own (gate, softmax/top-k, capacity dispatch, expert FFNs in double,
+    combine).  Host weights are drawn once, outside any timing."""
+
+    def __init__(self, cfg, T, seed):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.cfg, self.T = cfg, T
+        dt = synth.F16 if cfg.dtype == "f16" else synth.F32
+        self.x = synth.fill((T, cfg.d), dt, seed, synth.TID_TOKENS, cfg.tok_sigma)
+        cs = synth.gate_col_scale(cfg, seed)
+        self.Wg = synth.fill((cfg.d, cfg.E), synth.F32, seed, synth.TID_WG, cfg.w_sigma, col_scale=cs)
+        self.w1, self.w2 = synth.expert_slices(cfg, range(cfg.E), seed)
+        self.Wr1 = self.Wr2 = None
+        if cfg.residual:
+            self.Wr1 = synth.fill((cfg.d, cfg.f_res), dt, seed, synth.TID_WR1, cfg.w_sigma)
+            self.Wr2 = synth.fill((cfg.f_res, cfg.d), dt, seed, synth.TID_WR2, cfg.w_sigma)
+        self.cf = float(np.float32(cfg.cf))
+        self.pos = 0
+
+    def run(self, n):
+        n = max(1, min(n, self.T))
+        if self.pos + n > self.T:
+            self.pos = 0
+        x = self.x[self.pos:self.pos + n]
+        self.pos += n
+        t0 = time.perf_counter()
+        self.oracle.layer_forward(x, self.Wg, self.w1, self.w2, self.cfg.k, self.cf, self.Wr1,
+                                  self.Wr2)
+        return time.perf_counter() - t0
+
+    def size_for(self, seconds):
+        """Sub-batch size that takes about `seconds` (calibrated on one small call)."""
+        per_tok = self.run(8) / 8
+        return max(1, min(self.T, int(seconds / per_tok)))
+
+    def describe(self, n, steps):
+        return (f"{steps} sub-batch(es) of {n} contiguous tokens from the T={self.T} batch, each "
+                f"a full oracle layer call (own routing and capacity), host weights drawn untimed")
+
+
+def oracle_tokens_per_s(cfg, T, seed, budget_s):
+    r = OracleRunner(cfg, T, seed)
+    n = r.size_for(budget_s / 4)
+    spent, done, steps = 0.0, 0, 0
+    while spent < budget_s * 0.75 and steps < 64:
+        spent += r.run(n)
+        done += n
+        steps += 1
+    return done / spent, r.oracle.num_threads(), r.describe(n, steps) + f", {spent:.1f} s"
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg, T = synth.workload(args.workload, args.tokens)
+    K, W = args.steps, args.warmup
+    r = OracleRunner(cfg, T, args.seed)
+    n = r.size_for(min(5.0, 150.0 / max(1, K + W)))
+    for _ in range(W):
+        r.run(n)
+    t0 = time.perf_counter()
+    busy = 0.0
+    for _ in range(K):
+        busy += r.run(n)
+    elapsed = time.perf_counter() - t0
+    rate = n * K / busy
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": K, "warmup": W, "ms_per_step": 1000.0 * elapsed / max(1, K),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "T": T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
+                   "capacity_factor": cfg.cf},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": r.oracle.num_threads(),
+                         "kind": "oracle", "sample": r.describe(n, K)},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------ GPU arm
+def traffic_record(kernel_file):
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    src = open(kernel_file, "rb").read()
+    if rec.get("kernel_sha256") != hashlib.sha256(src).hexdigest():
+        return None
+    return rec
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_expert_ffn_layer_gb300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    cfg, T = synth.workload(args.workload, args.tokens)
+    seed = args.seed + 1000 * rank
+    f16 = cfg.dtype == "f16"
+    tdt = torch.float16 if f16 else torch.float32
+    n_batches = 4
+    W1 = torch.empty((cfg.E, cfg.d, cfg.f), dtype=tdt, device="cuda")
+    W2 = torch.empty((cfg.E, cfg.f, cfg.d), dtype=tdt, device="cuda")
+    synth.fill_cuda(W1, seed, synth.TID_W1, cfg.w_sigma)
+    synth.fill_cuda(W2, seed, synth.TID_W2, cfg.w_sigma)
+    cs = synth.gate_col_scale(cfg, seed)
+    Wg = torch.from_numpy(synth.fill((cfg.d, cfg.E), synth.F32, seed, synth.TID_WG, cfg.w_sigma,
+                                     col_scale=cs)).cuda()
+    Wr1 = Wr2 = None
+    if cfg.residual:
+        Wr1 = torch.empty((cfg.d, cfg.f_res), dtype=tdt, device="cuda")
+        Wr2 = torch.empty((cfg.f_res, cfg.d), dtype=tdt, device="cuda")
+        synth.fill_cuda(Wr1, seed, synth.TID_WR1, cfg.w_sigma)
+        synth.fill_cuda(Wr2, seed, synth.TID_WR2, cfg.w_sigma)
+    host_tok = [torch.from_numpy(synth.fill((T, cfg.d), synth.F16 if f16 else synth.F32, seed,
+                                            synth.TID_TOKENS + (b << 8), cfg.tok_sigma)).pin_memory()
+                for b in range(n_batches)]
+    dev_tok = [h.cuda() for h in host_tok]
+    out = torch.empty((T, cfg.d), dtype=tdt, device="cuda")
+    host_out = torch.empty((T, cfg.d), dtype=tdt).pin_memory()
+    mlp = moe.MOE_MLP_RESIDUAL if cfg.residual else moe.MOE_MLP_STANDARD
+    ws = torch.empty(moe.moe_workspace_size(T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.cf, mlp, cfg.f_res,
+                                            moe.MOE_F16 if f16 else moe.MOE_F32),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(tok, idx=None, slot=None):
+        moe.moe_layer_forward(tok, Wg, W1, W2, cfg.k, cfg.cf, out, ws, mlp_type=mlp, Wr1=Wr1,
+                              Wr2=Wr2, topk_idx_out=idx, slot_of_out=slot)
+
+    # routing statistics of each batch (for the algorithmic byte and FLOP counts)
+    stats = []
+    idx = torch.empty((T, cfg.k), dtype=torch.int32, device="cuda")
+    slot = torch.empty((T, cfg.k), dtype=torch.int32, device="cuda")
+    for b in range(n_batches):
+        step(dev_tok[b], idx, slot)
+        i_np, s_np = idx.cpu().numpy(), slot.cpu().numpy()
+        kept_mask = s_np >= 0
+        active = len(np.unique(i_np[kept_mask]))
+        stats.append((active, int(kept_mask.sum())))
+    if moe.moe_status_read(ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after the routing pass")
+    A = float(np.mean([s[0] for s in stats]))
+    S = float(np.mean([s[1] for s in stats]))
+
+    for i in range(args.warmup):
+        step(dev_tok[i % n_batches])
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_STAGE_EVENTS)]
+           for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(K):
+        moe.moe_set_stage_events(evs[i])
+        step(dev_tok[i % n_batches])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    moe.moe_set_stage_events(None)
+    if world > 1:
+        dist.barrier()
+    clocks.stop()
+    status = moe.moe_status_read(ws)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device status {moe.moe_status_string(status)}")
+    ms = e0.elapsed_time(e1)
+    stage_ms = np.zeros(moe.MOE_STAGE_EVENTS - 1)
+    for i in range(K):
+        for j in range(moe.MOE_STAGE_EVENTS - 1):
+            stage_ms[j] += evs[i][j].elapsed_time(evs[i][j + 1])
+    stage_ms /= K
+
+    # end to end through the public API with host buffers: H2D tokens, forward, D2H output
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dev_in = torch.empty_like(dev_tok[0])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    h0.record(stream)
+    for i in range(K):
+        dev_in.copy_(host_tok[i % n_batches], non_blocking=True)
+        step(dev_in)
+        host_out.copy_(out, non_blocking=True)
+    h1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = h0.elapsed_time(h1)
+
+    if world > 1:
+        t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    value = world * T * K / (ms / 1000.0)
+    value_e2e = world * T * K / (ms_e2e / 1000.0)
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    el = 2 if f16 else 4
+    # algorithmic bytes per launch: the active experts' weights once, plus activations
+    bytes_g1 = A * cfg.d * cfg.f * el + T * cfg.d * el
+    bytes_g2 = A * cfg.f * cfg.d * el + T * cfg.d * el
+    if cfg.residual:
+        bytes_g1 += cfg.d * cfg.f_res * el
+        bytes_g2 += cfg.f_res * cfg.d * el
+    g1_ms, g2_ms = stage_ms[3], stage_ms[4]
+    dom = "g1" if g1_ms >= g2_ms else "g2"
+    dom_bytes, dom_ms = (bytes_g1, g1_ms) if dom == "g1" else (bytes_g2, g2_ms)
+    achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
+    kernel_file = os.path.join(ROOT, "sparse_expert_ffn_layer_gb300", "csrc", "grouped_gemm.cu")
+    trec = traffic_record(kernel_file)
+    traffic = None
+    if trec is not None and trec.get("workload") == f"{cfg.name}:T{T}":
+        traffic = trec.get("per_launch_bytes", {}).get(dom)
+    # whole-layer roofline
+    layer_bytes = bytes_g1 + bytes_g2 + cfg.d * cfg.E * 4
+    layer_flops = 4.0 * cfg.d * cfg.f * S + 2.0 * T * cfg.d * cfg.E + \
+        (4.0 * T * cfg.d * cfg.f_res if cfg.residual else 0.0)
+    t_roof = max(layer_bytes / (hbm * 1e9), layer_flops / (bf16 * 1e12))
+    launches_per_step = 5 + (1 if (cfg.k == 2 or cfg.residual) else 0)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16" if f16 else "f32",
+        "data": "synthetic (seeded counter-based draws; 4 token batches cycled)",
+        "config": {"workload": f"{cfg.name}: 350M+MoE-128 layer" if cfg.name == "moe350m_e128"
+                   else cfg.name, "T": T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
+                   "capacity_factor": cfg.cf, "mlp_type": "residual" if cfg.residual else "standard",
+                   "l2": f"inputs larger than L2: {2 * cfg.E * cfg.d * cfg.f * el / 1e9:.2f} GB of "
+                         "expert weights per step vs 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "kernel": "grouped_gemm_kernel (expert GEMM1 + GeLU)" if dom == "g1"
+                     else "grouped_gemm_kernel (expert GEMM2 + combine)",
+                     "peak_source": peak_src},
+        "layer_roofline": {"bound": "hbm" if layer_bytes / (hbm * 1e9) >= layer_flops / (bf16 * 1e12)
+                           else "tensor", "roofline_ms": t_roof * 1000, "frac": t_roof * 1000 / (ms / K),
+                           "bytes": layer_bytes, "flops": layer_flops},
+        "stage_ms": {name: float(v) for name, v in zip(moe.STAGES, stage_ms)},
+        "routing": {"active_experts": A, "kept_slots": S},
+        "e2e": {"value": value_e2e, "unit": UNIT, "h2d_bytes_per_step": T * cfg.d * el,
+                "d2h_bytes_per_step": T * cfg.d * el},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        rate, cores, desc = oracle_tokens_per_s(cfg, T, seed, args.cpu_budget_s)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

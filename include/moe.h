@@ -1,0 +1,207 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) gated Mixture-of-Experts FFN layer, forward pass.
+ *
+ * One layer, one GPU, every expert resident in device memory:
+ *
+ *   gate      logits[t,e] = sum_i x[t,i] Wg[i,e] (fp32), softmax over experts, top-1 or
+ *             top-2 by logit.  Each token is sent to experts by a gating function
+ *             (DeepSpeed-MoE review, "MoE based NLG Model Architecture").
+ *   dispatch  capacity C = ceil(cf T / E) per expert; assignments taken in token order,
+ *             those past an expert's capacity are dropped; compact slots per expert.
+ *   experts   FFN_e(x) = GeLU_tanh(x W1[e]) W2[e], fp16 operands, fp32 accumulation.
+ *   combine   out[t] = sum_j w[t,j] FFN_{e_j}(x_t) over kept assignments: Top2-MoE sums the
+ *             outputs of two experts (same review, "Phenomenon2").
+ *   residual  mlp_type 'residual' (DeepSpeed-MoE Inference wiki, "PR-MoE 최적화로 더 낮은 비용";
+ *             PR-MoE in the review) adds a fixed dense MLP GeLU(x Wr1) Wr2 to the routed
+ *             expert's output (review, "Phenomenon2": Residual-MoE).
+ *
+ * The pages fix none of the exact formulas; the readings used are stated beside each call
+ * (no biases; fp32 fused-multiply-add chain for the logits; ties go to the lower expert
+ * index; top-1 weight = softmax probability of the chosen expert; top-2 weights are the two
+ * probabilities renormalised to sum 1 before drops and not after; capacity independent of
+ * k; dropped assignments contribute zero; GeLU in its tanh form).
+ *
+ * Conventions for every call:
+ *   - Matrices are dense row-major.  Shapes are given as [rows, cols].
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.  The
+ *     library never allocates or frees device memory, keeps no pointer after a call
+ *     returns, and never synchronises `stream` (moe_status_read excepted).
+ *   - All work is enqueued on `stream` (a cudaStream_t; 0 is the legacy default stream);
+ *     calls return once the work is enqueued.
+ *   - Return value: a moe_status.  Argument errors are detected on the host before anything
+ *     is enqueued, and nothing is written then.  MOE_ERR_CUDA reports a failed launch.
+ *     Errors found on the device while a call runs (a bounded wait that gave up) are
+ *     recorded in the workspace's status word and read with moe_status_read.
+ *   - No call throws across this boundary; all are safe to call from any host thread as
+ *     long as concurrent calls use different workspaces and outputs.
+ *   - T = 0 (an empty batch) is valid: the call enqueues nothing and returns MOE_OK.
+ *
+ * Supported shapes: E <= 1024, k in {1, 2}, k <= E.  MOE_F16 (tensor-core path): d, f and
+ * f_res multiples of 128.  MOE_F32 (SIMT path): d and f multiples of 4.  Every pointer
+ * 16-byte aligned.  Otherwise MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* a size, pointer, k, capacity factor or enum is invalid */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid, but a shape / alignment this build does not run */
+  MOE_ERR_WORKSPACE = 3,      /* workspace missing or smaller than moe_workspace_size */
+  MOE_ERR_CUDA = 4,           /* a CUDA launch or API call failed */
+  MOE_ERR_TIMEOUT = 5,        /* device side: a bounded wait gave up (status word) */
+  MOE_ERR_DEVICE_BOUNDS = 6   /* device side: an index failed its bounds check (status word) */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_F16 = 1 } moe_dtype;           /* activations and expert weights */
+typedef enum { MOE_MLP_STANDARD = 0, MOE_MLP_RESIDUAL = 1 } moe_mlp_type;
+
+/*
+ * Capacity per expert: C = ceil(cf * T / E), with cf*T and the division evaluated in
+ * double.  The pages name an expert's capacity (DeepSpeed-MoE review, "Phenomenon2") but
+ * give no formula; this is the capacity-factor definition.  Host only.
+ * Returns C (0 when T = 0), or -1 when T < 0, E < 1, cf <= 0 / not finite, or C > 2^31-1.
+ */
+MOE_API int moe_capacity(int T, int E, float capacity_factor);
+
+/*
+ * Bytes of workspace that moe_layer_forward needs for this shape (and enough for
+ * moe_expert_ffn of the same shape).  Host only; writes *bytes.  f_res is ignored for
+ * MOE_MLP_STANDARD.  Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED as the calls would.
+ */
+MOE_API moe_status moe_workspace_size(int T, int d, int f, int E, int k, float capacity_factor,
+                              moe_mlp_type mlp_type, int f_res, moe_dtype dtype, size_t* bytes);
+
+/*
+ * Gate: logits, softmax and top-k (DeepSpeed-MoE review, "MoE based NLG Model
+ * Architecture": tokens reach experts through a gating function; "Phenomenon2": Top2).
+ *   tokens     [T, d] in `dtype` (f16 values are widened exactly to f32).
+ *   Wg         [d, E] float32.
+ *   logits_in  nullable [T, E] float32: when given, the logits are taken from here and
+ *              tokens / Wg are not read (may be NULL then).
+ *   logits_out [T, E] float32: the logits used; required when logits_in is NULL (it holds
+ *              them), otherwise nullable (a copy of logits_in).
+ *   probs_out  nullable [T, E] float32: softmax over E.
+ *   topk_idx   [T, k] int32: experts by descending logit, ties to the lower index.
+ *   topk_w     [T, k] float32: k = 1: p[e1]; k = 2: p[e_j] / (p[e1] + p[e2]).
+ * The logits are the fp32 chain acc = fmaf(x[t,i], Wg[i,e], acc), i ascending from +0, so
+ * they (and hence routing) are reproducible bit for bit by any IEEE implementation.
+ */
+MOE_API moe_status moe_gate_topk(const void* tokens, moe_dtype dtype, const float* Wg,
+                                 const float* logits_in, int T, int d, int E, int k, float* logits_out,
+                         float* probs_out, int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
+/*
+ * Capacity-limited dispatch (reading: token-major order, capacity ceil(cf T / E)).
+ *   topk_idx   [T, k] int32 experts (values outside [0, E) are out of contract).
+ *   counts_raw [E]    assignments per expert before the capacity cut.
+ *   kept       [E]    min(counts_raw, C).
+ *   offsets    [E+1]  exclusive scan of kept; offsets[E] = S, the number of kept slots.
+ *   perm       [min(T k, E C)]  perm[s] = token of slot s; expert e owns slots
+ *                               offsets[e] .. offsets[e+1]-1 in token order.  Entries >= S
+ *                               are not written.
+ *   slot_of    [T, k] slot of assignment (t, j), or -1 when it was dropped.
+ * Pure integer work: results are unique and bit-exact.  One thread block; no atomics.
+ */
+MOE_API moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k, float capacity_factor,
+                        int32_t* counts_raw, int32_t* kept, int32_t* offsets, int32_t* perm,
+                        int32_t* slot_of, moe_stream_t stream);
+
+/*
+ * Grouped expert FFN over the dispatched slots, unscaled:
+ *   expert_out[s, :] = GeLU_tanh(tokens[perm[s], :] W1[e]) W2[e]   for s in expert e's slots.
+ *   tokens [T, d], W1 [E, d, f], W2 [E, f, d], expert_out [S_max, d]: all in `dtype`.
+ *   perm, offsets: as written by moe_dispatch.  S_max >= offsets[E] bounds the slot count
+ *   (min(T k, E C) always suffices).  Rows >= offsets[E] of expert_out are not written.
+ *   workspace: >= 256 + S_max * f * sizeof(dtype) bytes, rounded up to a multiple of 256
+ *   (the status word, then the hidden activations H [S_max, f]); moe_workspace_size of the
+ *   same layer shape is always enough for S_max = min(T k, E C).
+ * f16: hidden activations are rounded to f16 between the two GEMMs.
+ */
+MOE_API moe_status moe_expert_ffn(const void* tokens, const int32_t* perm, const int32_t* offsets,
+                          const void* W1, const void* W2, moe_dtype dtype, int T, int d, int f,
+                          int E, int S_max, void* expert_out, void* workspace, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/*
+ * Gate-weighted combine back to token order (DeepSpeed-MoE review, "Phenomenon2": the
+ * outputs of the experts a token visits are summed; Residual-MoE adds a fixed MLP):
+ *   out[t, :] = sum_j [slot_of[t,j] >= 0] topk_w[t,j] expert_out[slot_of[t,j], :]
+ *               (+ residual_in[t, :] when residual_in is not NULL)
+ * in fp32, j ascending, the residual added last, rounded once to `dtype`.
+ *   expert_out [S, d], residual_in nullable [T, d], out [T, d]: all in `dtype`.
+ */
+MOE_API moe_status moe_combine(const void* expert_out, const int32_t* slot_of, const float* topk_w,
+                       const void* residual_in, moe_dtype dtype, int T, int d, int k, void* out,
+                       moe_stream_t stream);
+
+/*
+ * The whole layer, fused: gate, dispatch, expert GEMM1 + GeLU, expert GEMM2 with the
+ * gate-weighted combine in its epilogue, and for MOE_MLP_RESIDUAL the dense MLP
+ *   out[t] += GeLU(x_t Wr1) Wr2,   Wr1 [d, f_res], Wr2 [f_res, d]   (NULL for STANDARD),
+ * computed by the same grouped-GEMM kernels as an extra group of all T tokens.
+ *   tokens [T, d], W1 [E, d, f], W2 [E, f, d], out [T, d]: `dtype`.  Wg [d, E]: float32.
+ *   topk_idx_out nullable [T, k], slot_of_out nullable [T, k]: routing, as moe_gate_topk /
+ *   moe_dispatch define it.
+ *   workspace >= moe_workspace_size(...) bytes; contents need no initialisation.
+ * Deterministic: repeated calls give identical bits (fp32 sums of at most two addends
+ * commute exactly; larger sums use a fixed order).
+ */
+MOE_API moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1, const void* W2,
+                             const void* Wr1, const void* Wr2, moe_dtype dtype, int T, int d,
+                             int f, int E, int k, float capacity_factor, moe_mlp_type mlp_type,
+                             int f_res, void* out, int32_t* topk_idx_out, int32_t* slot_of_out,
+                             void* workspace, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the device-side status word of the most recent
+ * moe_expert_ffn / moe_layer_forward call on this workspace (MOE_OK, MOE_ERR_TIMEOUT or
+ * MOE_ERR_DEVICE_BOUNDS), or MOE_ERR_CUDA if the synchronisation or the read failed.
+ * The word is cleared at the start of each of those calls.
+ */
+MOE_API moe_status moe_status_read(const void* workspace, moe_stream_t stream);
+
+/* Static, human-readable name of a status code ("MOE_OK", ...). */
+MOE_API const char* moe_status_string(moe_status status);
+
+/*
+ * Self-test of the device-side bounded wait that every pipeline wait in the library uses:
+ * launches one block that waits on an mbarrier nothing ever arrives on, with a budget of
+ * timeout_ns nanoseconds (1 .. 10^10) instead of the library's default of 2 s.  The wait
+ * gives up, records MOE_ERR_TIMEOUT in the workspace's status word and the kernel returns
+ * normally, leaving the context usable; read the result with moe_status_read.
+ * workspace: >= 256 bytes.
+ */
+MOE_API moe_status moe_selftest_wait(void* workspace, uint64_t timeout_ns, moe_stream_t stream);
+
+/*
+ * Measurement hook (the pages have no counterpart): when `events` is not NULL, the calling
+ * thread's next moe_layer_forward calls record events[0 .. 6] (cudaEvent_t handles created
+ * by the caller) on their stream at the stage boundaries: [0] start, [1] after the gate
+ * logits, [2] after softmax / top-k, [3] after dispatch, [4] after the first expert GEMM
+ * (+ GeLU), [5] after the second expert GEMM (+ combine), [6] at the end.  n_events must be
+ * 7, or 0 with events NULL to stop recording.  Thread-local; host only.
+ */
+#define MOE_STAGE_EVENTS 7
+MOE_API moe_status moe_set_stage_events(void* const* events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

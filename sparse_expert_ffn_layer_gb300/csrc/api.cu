@@ -1,0 +1,504 @@
+// C-ABI front end (include/moe.h): argument checks, workspace carving, TMA descriptors and the
+// launch sequence of each entry point.  All device work is in the kernels of this library.
+#include <math.h>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "launch.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxE = 1024;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int capacity_of(int T, int E, float cf) {
+  if (T < 0 || E < 1 || !(cf > 0.0f) || isinf(cf)) return -1;
+  if (T == 0) return 0;
+  double c = ceil((double)cf * (double)T / (double)E);
+  if (c > 2147483647.0) return -1;
+  return (int)c;
+}
+
+// ---------------------------------------------------------------- workspace layout
+struct Ws {
+  size_t status, logits, topk_idx, topk_w, counts, kept, offsets, perm, slot_w, slot_of, H, Hres,
+      acc32, r32, total;
+};
+
+Ws ws_layout(int T, int d, int f, int E, int k, int C, bool residual, int f_res, bool f16) {
+  const size_t elt = f16 ? 2 : 4;
+  const size_t S_max = (size_t)std::min<long long>((long long)T * k, (long long)E * C);
+  const bool accum = k == 2 || residual;
+  Ws w;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  w.status = take(kAlign);
+  w.H = take(std::max<size_t>(S_max, 1) * f * elt);
+  w.logits = take((size_t)T * E * 4);
+  w.topk_idx = take((size_t)T * k * 4);
+  w.topk_w = take((size_t)T * k * 4);
+  w.counts = take((size_t)E * 4);
+  w.kept = take((size_t)E * 4);
+  w.offsets = take((size_t)(E + 1) * 4);
+  w.perm = take(std::max<size_t>(S_max, 1) * 4);
+  w.slot_w = take(std::max<size_t>(S_max, 1) * 4);
+  w.slot_of = take((size_t)T * k * 4);
+  w.Hres = residual ? take((size_t)T * f_res * elt) : 0;
+  w.acc32 = accum ? take((size_t)T * d * 4) : 0;
+  w.r32 = residual ? take((size_t)T * d * 4) : 0;
+  w.total = off;
+  return w;
+}
+
+size_t expert_ffn_ws_bytes(int S_max, int f, bool f16) {
+  return kAlign + align_up(std::max<size_t>((size_t)S_max, 1) * f * (f16 ? 2 : 4));
+}
+
+// ---------------------------------------------------------------- argument checks
+moe_status check_shape(int T, int d, int f, int E, int k, moe_dtype dtype) {
+  if (T < 0 || d < 1 || f < 1 || E < 1 || (k != 1 && k != 2) || k > E) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if ((long long)T * k > 0x7fffffffLL || (long long)T * E > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+  if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_F16 && (d % 128 || f % 128)) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_F32 && (d % 4 || f % 4)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------- device properties
+struct Dev {
+  int sms = 0, smem_optin = 0;
+};
+
+bool dev_props(Dev* out) {
+  static std::mutex mu;
+  static Dev cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!have[dev]) {
+    Dev p;
+    if (cudaDeviceGetAttribute(&p.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&p.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      return false;
+    cache[dev] = p;
+    have[dev] = true;
+  }
+  *out = cache[dev];
+  return true;
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D f16 row-major tensor [outer, inner] with a {box_inner, box_outer} box, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint32_t pow2_at_least(uint32_t v) {
+  uint32_t p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+// Plan of the two tensor-core launches for groups whose tiles hold <= rows_bound rows.
+struct TcPlan {
+  int nmax, stages, grid;
+  uint32_t acc_cols;
+};
+
+bool tc_plan(int rows_bound, int E, TcPlan* p) {
+  Dev dv;
+  if (!dev_props(&dv)) return false;
+  p->nmax = std::min(256, std::max(16, (rows_bound + 15) / 16 * 16));
+  p->acc_cols = pow2_at_least((uint32_t)p->nmax);
+  p->stages = gemm_stages_for(p->nmax, E, dv.smem_optin);
+  p->grid = dv.sms;
+  return p->stages >= 2;
+}
+
+// A (M-major weights) descriptor offsets for the 128-byte swizzle layout that two 64-wide
+// TMA boxes of 64 K-rows produce: M-blocks 8 KB apart, 8-row K groups 1 KB apart.
+constexpr uint32_t kALbo = 8192, kASbo = 1024;
+
+void fill_common(GemmArgs& g, const TcPlan& p, int E, int* status) {
+  memset(&g, 0, sizeof(g));
+  g.E = E;
+  g.nmax = p.nmax;
+  g.stages = p.stages;
+  g.acc_cols = p.acc_cols;
+  g.a_lbo = kALbo;
+  g.a_sbo = kASbo;
+  g.status = status;
+  g.wait_ns = kDefaultWaitNs;
+}
+
+thread_local cudaEvent_t* t_stage_events = nullptr;
+thread_local cudaEvent_t t_stage_store[MOE_STAGE_EVENTS];
+
+cudaError_t stage_mark(int i, cudaStream_t s) {
+  return t_stage_events ? cudaEventRecord(t_stage_events[i], s) : cudaSuccess;
+}
+
+#define MOE_TRY(expr)                          \
+  do {                                         \
+    cudaError_t e__ = (expr);                  \
+    if (e__ != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+// Expert FFN stage (both GEMMs) on the tensor cores.
+moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* offsets,
+                      const void* W1, const void* W2, const void* Wr1, const void* Wr2, int T,
+                      int d, int f, int E, int f_res, int S_rows, int rows_bound, __half* H,
+                      __half* Hres, int mode, void* out, float* acc32, float* r32,
+                      const float* slot_w, const int32_t* drop_slot_of, int* status,
+                      cudaStream_t s) {
+  const bool residual = Wr1 != nullptr;
+  TcPlan plan;
+  if (!tc_plan(rows_bound, E, &plan)) return MOE_ERR_CUDA;
+  CUtensorMap mW1, mX, mWr1, mW2, mH, mWr2, mHres;
+  const int S_dim = std::max(S_rows, 1);
+  if (!make_map(&mW1, W1, f, (uint64_t)E * d, 64, 64) || !make_map(&mX, tokens, d, T, 64, 1) ||
+      !make_map(&mW2, W2, d, (uint64_t)E * f, 64, 64) || !make_map(&mH, H, f, S_dim, 64, 16))
+    return MOE_ERR_CUDA;
+  if (residual) {
+    if (!make_map(&mWr1, Wr1, f_res, d, 64, 64) || !make_map(&mWr2, Wr2, d, f_res, 64, 64) ||
+        !make_map(&mHres, Hres, f_res, T, 64, 16))
+      return MOE_ERR_CUDA;
+  } else {
+    mWr1 = mW1;
+    mWr2 = mW2;
+    mHres = mH;
+  }
+  GemmArgs g1;
+  fill_common(g1, plan, E, status);
+  g1.offsets = offsets;
+  g1.perm = perm;
+  g1.n_res_rows = residual ? T : 0;
+  g1.K = d;
+  g1.K_res = d;
+  g1.mt_exp = f / 128;
+  g1.mt_res = residual ? f_res / 128 : 1;
+  g1.a_rows_per_expert = d;
+  g1.h_out = H;
+  g1.ldh = f;
+  g1.hres_out = Hres;
+  g1.ldhres = f_res;
+  if (mode == kModeAccum) {
+    g1.zero_f32 = acc32;
+    g1.zero_f32_n = (size_t)T * d;
+  }
+  if (mode == kModeDirect && drop_slot_of) {
+    g1.drop_slot_of = drop_slot_of;
+    g1.drop_T = T;
+    g1.drop_out = static_cast<__half*>(out);
+    g1.drop_d = d;
+  }
+  MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan.grid, s));
+  MOE_TRY(stage_mark(4, s));
+
+  GemmArgs g2;
+  fill_common(g2, plan, E, status);
+  g2.offsets = offsets;
+  g2.perm = perm;
+  g2.n_res_rows = residual ? T : 0;
+  g2.K = f;
+  g2.K_res = f_res;
+  g2.mt_exp = d / 128;
+  g2.mt_res = d / 128;
+  g2.a_rows_per_expert = f;
+  g2.mode = mode;
+  g2.out = static_cast<__half*>(out);
+  g2.acc32 = acc32;
+  g2.r32 = r32;
+  g2.ldo = d;
+  g2.slot_w = slot_w;
+  MOE_TRY(launch_grouped_gemm2(mW2, mH, mWr2, mHres, g2, plan.grid, s));
+  MOE_TRY(stage_mark(5, s));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_capacity(int T, int E, float capacity_factor) { return capacity_of(T, E, capacity_factor); }
+
+moe_status moe_workspace_size(int T, int d, int f, int E, int k, float capacity_factor,
+                              moe_mlp_type mlp_type, int f_res, moe_dtype dtype, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_shape(T, d, f, E, k, dtype);
+  if (st != MOE_OK) return st;
+  if (mlp_type != MOE_MLP_STANDARD && mlp_type != MOE_MLP_RESIDUAL) return MOE_ERR_INVALID_ARG;
+  const bool residual = mlp_type == MOE_MLP_RESIDUAL;
+  if (residual && f_res < 1) return MOE_ERR_INVALID_ARG;
+  if (residual && dtype == MOE_F16 && f_res % 128) return MOE_ERR_UNSUPPORTED;
+  if (residual && dtype == MOE_F32 && f_res % 4) return MOE_ERR_UNSUPPORTED;
+  const int C = capacity_of(T, E, capacity_factor);
+  if (C < 0) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(T, d, f, E, k, C, residual, residual ? f_res : 0, dtype == MOE_F16).total;
+  return MOE_OK;
+}
+
+moe_status moe_gate_topk(const void* tokens, moe_dtype dtype, const float* Wg,
+                         const float* logits_in, int T, int d, int E, int k, float* logits_out,
+                         float* probs_out, int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
+  if (T < 0 || d < 1 || E < 1 || (k != 1 && k != 2) || k > E) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (!topk_idx || !topk_w || (!logits_in && (!tokens || !Wg))) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || (long long)T * E > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(tokens) || !aligned16(Wg) || !aligned16(logits_in) || !aligned16(logits_out) ||
+      !aligned16(probs_out) || !aligned16(topk_idx) || !aligned16(topk_w))
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (logits_in) {
+    MOE_TRY(launch_softmax_topk(logits_in, T, E, k, probs_out, topk_idx, topk_w, logits_out, s));
+  } else {
+    if (!logits_out) return MOE_ERR_INVALID_ARG;   // the logits need a home
+    MOE_TRY(launch_gate_logits(tokens, dtype == MOE_F16, Wg, T, d, E, logits_out, s));
+    MOE_TRY(launch_softmax_topk(logits_out, T, E, k, probs_out, topk_idx, topk_w, nullptr, s));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k, float capacity_factor,
+                        int32_t* counts_raw, int32_t* kept, int32_t* offsets, int32_t* perm,
+                        int32_t* slot_of, moe_stream_t stream) {
+  if (T < 0 || E < 1 || (k != 1 && k != 2) || k > E) return MOE_ERR_INVALID_ARG;
+  const int C = capacity_of(T, E, capacity_factor);
+  if (C < 0) return MOE_ERR_INVALID_ARG;
+  if (!topk_idx || !counts_raw || !kept || !offsets || !perm || !slot_of) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || (long long)T * k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  MOE_TRY(launch_dispatch(topk_idx, T, k, E, C, counts_raw, kept, offsets, perm, slot_of, nullptr,
+                          nullptr, reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const void* tokens, const int32_t* perm, const int32_t* offsets,
+                          const void* W1, const void* W2, moe_dtype dtype, int T, int d, int f,
+                          int E, int S_max, void* expert_out, void* workspace, size_t ws_bytes,
+                          moe_stream_t stream) {
+  moe_status st = check_shape(T, d, f, E, 1, dtype);
+  if (st != MOE_OK) return st;
+  if (S_max < 0) return MOE_ERR_INVALID_ARG;
+  if (!tokens || !perm || !offsets || !W1 || !W2 || !expert_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(tokens) || !aligned16(W1) || !aligned16(W2) || !aligned16(expert_out) ||
+      !aligned16(workspace))
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0 || S_max == 0) return MOE_OK;
+  const bool f16 = dtype == MOE_F16;
+  if (!workspace || ws_bytes < expert_ffn_ws_bytes(S_max, f, f16)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  MOE_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  if (f16) {
+    return run_tc_ffn(tokens, perm, offsets, W1, W2, nullptr, nullptr, T, d, f, E, 0, S_max, S_max,
+                      reinterpret_cast<__half*>(ws + kAlign), nullptr, kModeExpertOut, expert_out,
+                      nullptr, nullptr, nullptr, nullptr, status, s);
+  }
+  SimtArgs a;
+  memset(&a, 0, sizeof(a));
+  a.x = static_cast<const float*>(tokens);
+  a.offsets = offsets;
+  a.perm = perm;
+  a.W1 = static_cast<const float*>(W1);
+  a.W2 = static_cast<const float*>(W2);
+  a.T = T; a.d = d; a.f = f; a.E = E;
+  a.H = reinterpret_cast<float*>(ws + kAlign);
+  a.mode = kModeExpertOut;
+  a.out = static_cast<float*>(expert_out);
+  MOE_TRY(launch_simt_ffn1(a, S_max, s));
+  MOE_TRY(launch_simt_ffn2(a, S_max, s));
+  return MOE_OK;
+}
+
+moe_status moe_combine(const void* expert_out, const int32_t* slot_of, const float* topk_w,
+                       const void* residual_in, moe_dtype dtype, int T, int d, int k, void* out,
+                       moe_stream_t stream) {
+  if (T < 0 || d < 1 || (k != 1 && k != 2)) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (!expert_out || !slot_of || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  MOE_TRY(launch_combine(expert_out, slot_of, topk_w, residual_in, dtype == MOE_F16, T, d, k, out,
+                         reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1, const void* W2,
+                             const void* Wr1, const void* Wr2, moe_dtype dtype, int T, int d,
+                             int f, int E, int k, float capacity_factor, moe_mlp_type mlp_type,
+                             int f_res, void* out, int32_t* topk_idx_out, int32_t* slot_of_out,
+                             void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_shape(T, d, f, E, k, dtype);
+  if (st != MOE_OK) return st;
+  if (mlp_type != MOE_MLP_STANDARD && mlp_type != MOE_MLP_RESIDUAL) return MOE_ERR_INVALID_ARG;
+  const bool residual = mlp_type == MOE_MLP_RESIDUAL;
+  const int C = capacity_of(T, E, capacity_factor);
+  if (C < 0) return MOE_ERR_INVALID_ARG;
+  if (!tokens || !Wg || !W1 || !W2 || !out) return MOE_ERR_INVALID_ARG;
+  if (residual && (!Wr1 || !Wr2 || f_res < 1)) return MOE_ERR_INVALID_ARG;
+  if (residual && ((dtype == MOE_F16 && f_res % 128) || (dtype == MOE_F32 && f_res % 4)))
+    return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(tokens) || !aligned16(Wg) || !aligned16(W1) || !aligned16(W2) || !aligned16(out) ||
+      !aligned16(workspace) || !aligned16(topk_idx_out) || !aligned16(slot_of_out) ||
+      (residual && (!aligned16(Wr1) || !aligned16(Wr2))))
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  const bool f16 = dtype == MOE_F16;
+  const Ws L = ws_layout(T, d, f, E, k, C, residual, residual ? f_res : 0, f16);
+  if (!workspace || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  float* logits = reinterpret_cast<float*>(ws + L.logits);
+  int32_t* topk_idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t*>(ws + L.topk_idx);
+  float* topk_w = reinterpret_cast<float*>(ws + L.topk_w);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  int32_t* kept = reinterpret_cast<int32_t*>(ws + L.kept);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
+  float* slot_w = reinterpret_cast<float*>(ws + L.slot_w);
+  int32_t* slot_of = slot_of_out ? slot_of_out : reinterpret_cast<int32_t*>(ws + L.slot_of);
+  float* acc32 = L.acc32 ? reinterpret_cast<float*>(ws + L.acc32) : nullptr;
+  float* r32 = L.r32 ? reinterpret_cast<float*>(ws + L.r32) : nullptr;
+  const int mode = (k == 1 && !residual) ? kModeDirect : kModeAccum;
+  const int S_max = (int)std::min<long long>((long long)T * k, (long long)E * C);
+
+  MOE_TRY(stage_mark(0, s));
+  MOE_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  MOE_TRY(launch_gate_logits(tokens, f16, Wg, T, d, E, logits, s));
+  MOE_TRY(stage_mark(1, s));
+  MOE_TRY(launch_softmax_topk(logits, T, E, k, nullptr, topk_idx, topk_w, nullptr, s));
+  MOE_TRY(stage_mark(2, s));
+  MOE_TRY(launch_dispatch(topk_idx, T, k, E, C, counts, kept, offsets, perm, slot_of, topk_w, slot_w,
+                          s));
+  MOE_TRY(stage_mark(3, s));
+  const int rows_bound = std::max(std::min(C, T * k), residual ? T : 0);
+  if (f16) {
+    st = run_tc_ffn(tokens, perm, offsets, W1, W2, residual ? Wr1 : nullptr, residual ? Wr2 : nullptr,
+                    T, d, f, E, residual ? f_res : 0, S_max, rows_bound,
+                    reinterpret_cast<__half*>(ws + L.H),
+                    residual ? reinterpret_cast<__half*>(ws + L.Hres) : nullptr, mode, out, acc32, r32,
+                    slot_w, k == 1 ? slot_of : nullptr, status, s);
+    if (st != MOE_OK) return st;
+  } else {
+    SimtArgs a;
+    memset(&a, 0, sizeof(a));
+    a.x = static_cast<const float*>(tokens);
+    a.offsets = offsets;
+    a.perm = perm;
+    a.W1 = static_cast<const float*>(W1);
+    a.W2 = static_cast<const float*>(W2);
+    a.Wr1 = residual ? static_cast<const float*>(Wr1) : nullptr;
+    a.Wr2 = residual ? static_cast<const float*>(Wr2) : nullptr;
+    a.T = T; a.d = d; a.f = f; a.E = E; a.f_res = residual ? f_res : 0;
+    a.H = reinterpret_cast<float*>(ws + L.H);
+    a.Hres = residual ? reinterpret_cast<float*>(ws + L.Hres) : nullptr;
+    a.mode = mode;
+    a.out = static_cast<float*>(out);
+    a.acc32 = acc32;
+    a.r32 = r32;
+    a.slot_w = slot_w;
+    if (mode == kModeDirect) MOE_TRY(launch_zero_dropped_rows(slot_of, T, k, d, 0, out, s));
+    else MOE_TRY(launch_zero_f32(acc32, (size_t)T * d, s));
+    MOE_TRY(launch_simt_ffn1(a, rows_bound, s));
+    MOE_TRY(stage_mark(4, s));
+    MOE_TRY(launch_simt_ffn2(a, rows_bound, s));
+    MOE_TRY(stage_mark(5, s));
+  }
+  if (mode == kModeAccum) MOE_TRY(launch_finalize(acc32, r32, T, d, f16, out, s));
+  MOE_TRY(stage_mark(6, s));
+  return MOE_OK;
+}
+
+moe_status moe_status_read(const void* workspace, moe_stream_t stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int v = -1;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v == MOE_OK || v == MOE_ERR_TIMEOUT || v == MOE_ERR_DEVICE_BOUNDS) return (moe_status)v;
+  return MOE_ERR_CUDA;
+}
+
+const char* moe_status_string(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status moe_set_stage_events(void* const* events, int n_events) {
+  if (events == nullptr && n_events == 0) {
+    t_stage_events = nullptr;
+    return MOE_OK;
+  }
+  if (events == nullptr || n_events != MOE_STAGE_EVENTS) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_STAGE_EVENTS; ++i) {
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+    t_stage_store[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  t_stage_events = t_stage_store;
+  return MOE_OK;
+}
+
+moe_status moe_selftest_wait(void* workspace, uint64_t timeout_ns, moe_stream_t stream) {
+  if (!workspace || timeout_ns < 1 || timeout_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(workspace);
+  MOE_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
+  MOE_TRY(launch_selftest_wait(status, timeout_ns, s));
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,136 @@
+// Capacity-limited dispatch: per-expert counts, exclusive scan, slot assignment in token
+// order, overflow dropped.
+//
+// Reading of the pages (which name expert capacity in the DeepSpeed-MoE review,
+// "Phenomenon2", without a rule): capacity C = ceil(cf T / E) per expert; the assignments
+// (t, j) are taken token-major; an assignment's rank is the number of earlier assignments
+// to the same expert; it is kept iff rank < C; expert e owns the compact slot range
+// offsets[e] .. offsets[e] + kept[e] - 1 in token order.
+//
+// One block of 32 warps, no atomics.  Warp w owns a contiguous run of the assignment list.
+// Pass 1: each warp walks its run 32 assignments at a time; lanes with equal experts are
+// grouped with __match_any_sync, so the rank inside the warp's run is the warp's running
+// count for that expert (in shared memory, private to the warp) plus the number of
+// lower lanes in the group.  Pass 2: per expert, an exclusive scan of the 32 warp counts
+// gives each warp's base; kept = min(count, C); a block scan of kept gives the offsets.
+// Pass 3: each assignment's global rank is base + local rank, which decides kept / dropped
+// and the slot.
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 32;
+
+__global__ void __launch_bounds__(1024) dispatch_kernel(
+    const int32_t* __restrict__ topk_idx, int n, int k, int E, int C,
+    int32_t* __restrict__ counts_raw, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm, int32_t* __restrict__ slot_of, const float* __restrict__ topk_w,
+    float* __restrict__ slot_w) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;                       // [kWarps][E]: running count, then warp base
+  int32_t* offs = sm + kWarps * E;         // [E + 1]
+  int32_t* wsum = offs + E + 1;            // [kWarps] scan scratch
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int q = threadIdx.x; q < kWarps * E; q += blockDim.x) cnt[q] = 0;
+  __syncthreads();
+
+  const int L = (n + kWarps - 1) / kWarps;
+  const int a_begin = min(n, w * L), a_end = min(n, a_begin + L);
+  const unsigned lt_mask = (1u << lane) - 1u;
+
+  // pass 1: rank inside the warp's run; kept temporarily in slot_of
+  for (int base = a_begin; base < a_end; base += 32) {
+    const int a = base + lane;
+    const bool valid = a < a_end;
+    const int e = valid ? topk_idx[a] : -1 - lane;     // invalid lanes form singleton groups
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    const int leader = __ffs(grp) - 1;
+    int before = 0;
+    if (valid) before = cnt[w * E + e];
+    __syncwarp();
+    if (valid) {
+      slot_of[a] = before + __popc(grp & lt_mask);
+      if (lane == leader) cnt[w * E + e] = before + __popc(grp);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // pass 2: per-expert scan over warps, kept, then a block scan of kept
+  int my_kept = 0;
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int run = 0;
+    for (int ww = 0; ww < kWarps; ++ww) {
+      int c = cnt[ww * E + e];
+      cnt[ww * E + e] = run;
+      run += c;
+    }
+    counts_raw[e] = run;
+    my_kept = min(run, C);
+    kept[e] = my_kept;
+  }
+  // block-wide exclusive scan of my_kept over threads 0 .. E-1 (E <= 1024)
+  int incl = my_kept;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = wsum[lane];
+    int s = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int u = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += u;
+    }
+    wsum[lane] = s - v;                  // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  if (threadIdx.x < E) {
+    int ex = wsum[w] + incl - my_kept;
+    offs[threadIdx.x] = ex;
+    offsets[threadIdx.x] = ex;
+    if (threadIdx.x == E - 1) {
+      offs[E] = ex + my_kept;
+      offsets[E] = ex + my_kept;
+    }
+  }
+  __syncthreads();
+
+  // pass 3: global rank -> slot
+  for (int a = a_begin + lane; a < a_end; a += 32) {
+    const int e = topk_idx[a];
+    const int r = cnt[w * E + e] + slot_of[a];
+    if (r < C) {
+      const int s = offs[e] + r;
+      slot_of[a] = s;
+      perm[s] = a / k;
+      if (slot_w) slot_w[s] = topk_w[a];
+    } else {
+      slot_of[a] = -1;
+    }
+  }
+}
+
+}  // namespace
+
+size_t dispatch_smem_bytes(int E) { return sizeof(int32_t) * ((size_t)kWarps * E + E + 1 + kWarps); }
+
+cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C, int32_t* counts_raw,
+                            int32_t* kept, int32_t* offsets, int32_t* perm, int32_t* slot_of,
+                            const float* topk_w, float* slot_w, cudaStream_t s) {
+  size_t smem = dispatch_smem_bytes(E);
+  cudaError_t err = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+  if (err != cudaSuccess) return err;
+  dispatch_kernel<<<1, kWarps * 32, smem, s>>>(topk_idx, T * k, k, E, C, counts_raw, kept, offsets,
+                                               perm, slot_of, topk_w, slot_w);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

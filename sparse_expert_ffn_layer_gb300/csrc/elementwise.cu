@@ -1,0 +1,163 @@
+// Bandwidth kernels around the expert GEMMs: clearing, the fp32 -> output conversion, the
+// standalone gate-weighted combine, and the bounded-wait self test.  Grids are sized in
+// multiples of the SM count and use 16-byte accesses where the row length allows.
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+int grid_for(size_t work, int per_block) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  size_t blocks = (work + per_block - 1) / per_block;
+  size_t cap = (size_t)sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return (int)blocks;
+}
+
+__global__ void zero_f32_kernel(float* __restrict__ p, size_t n) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t n4 = n / 4;
+  float4* p4 = reinterpret_cast<float4*>(p);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
+    p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (size_t i = n4 * 4 + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0.f;
+}
+
+// Rows of tokens none of whose assignments were kept become zero (standard top-1 output).
+__global__ void zero_dropped_rows_kernel(const int32_t* __restrict__ slot_of, int T, int k,
+                                         size_t row_bytes, uint8_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    bool any = false;
+    for (int j = 0; j < k; ++j) any |= slot_of[(size_t)t * k + j] >= 0;
+    if (any) continue;
+    uint4* row = reinterpret_cast<uint4*>(out + (size_t)t * row_bytes);
+    for (size_t c = lane; c < row_bytes / 16; c += 32) row[c] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+template <typename Tout>
+__device__ __forceinline__ Tout from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+
+template <typename Tv>
+__device__ __forceinline__ float as_f32(Tv v);
+template <>
+__device__ __forceinline__ float as_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float as_f32<__half>(__half v) { return __half2float(v); }
+
+// out = acc32 (+ r32), rounded once; four elements per thread step.
+template <typename Tout>
+__global__ void finalize_kernel(const float* __restrict__ acc32, const float* __restrict__ r32,
+                                size_t n, Tout* __restrict__ out) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n / 4; i += stride) {
+    float4 v = reinterpret_cast<const float4*>(acc32)[i];
+    if (r32) {
+      float4 r = reinterpret_cast<const float4*>(r32)[i];
+      v.x += r.x; v.y += r.y; v.z += r.z; v.w += r.w;
+    }
+    out[4 * i + 0] = from_f32<Tout>(v.x);
+    out[4 * i + 1] = from_f32<Tout>(v.y);
+    out[4 * i + 2] = from_f32<Tout>(v.z);
+    out[4 * i + 3] = from_f32<Tout>(v.w);
+  }
+}
+
+// out[t] = sum_j [slot >= 0] w_j expert_out[slot] (+ residual_in[t]); one warp per token row.
+template <typename T_>
+__global__ void combine_kernel(const T_* __restrict__ eo, const int32_t* __restrict__ slot_of,
+                               const float* __restrict__ topk_w, const T_* __restrict__ res,
+                               int T, int d, int k, T_* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    int s[2];
+    float w[2];
+    for (int j = 0; j < k; ++j) {
+      s[j] = slot_of[(size_t)t * k + j];
+      w[j] = topk_w[(size_t)t * k + j];
+    }
+    for (int c = lane; c < d; c += 32) {
+      float acc = 0.f;
+      for (int j = 0; j < k; ++j)
+        if (s[j] >= 0) acc += w[j] * as_f32<T_>(eo[(size_t)s[j] * d + c]);
+      if (res) acc += as_f32<T_>(res[(size_t)t * d + c]);
+      out[(size_t)t * d + c] = from_f32<T_>(acc);
+    }
+  }
+}
+
+__global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing arrives on `bar`: the wait must give up and record the timeout
+    mbar_wait_bounded(&bar, 0, &abort_flag, status, timeout_ns);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s) {
+  zero_f32_kernel<<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(p, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_dropped_rows(const int32_t* slot_of, int T, int k, int d, int dtype_f16,
+                                     void* out, cudaStream_t s) {
+  const size_t row_bytes = (size_t)d * (dtype_f16 ? 2 : 4);
+  zero_dropped_rows_kernel<<<grid_for((size_t)T * 32, 256), 256, 0, s>>>(
+      slot_of, T, k, row_bytes, static_cast<uint8_t*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* acc32, const float* r32, int T, int d, int dtype_f16,
+                            void* out, cudaStream_t s) {
+  const size_t n = (size_t)T * d;
+  const int g = grid_for(n / 4, 256);
+  if (dtype_f16) finalize_kernel<__half><<<g, 256, 0, s>>>(acc32, r32, n, static_cast<__half*>(out));
+  else finalize_kernel<float><<<g, 256, 0, s>>>(acc32, r32, n, static_cast<float*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* expert_out, const int32_t* slot_of, const float* topk_w,
+                           const void* residual_in, int dtype_f16, int T, int d, int k, void* out,
+                           cudaStream_t s) {
+  const int g = grid_for((size_t)T * 32, 256);
+  if (dtype_f16)
+    combine_kernel<__half><<<g, 256, 0, s>>>(static_cast<const __half*>(expert_out), slot_of, topk_w,
+                                             static_cast<const __half*>(residual_in), T, d, k,
+                                             static_cast<__half*>(out));
+  else
+    combine_kernel<float><<<g, 256, 0, s>>>(static_cast<const float*>(expert_out), slot_of, topk_w,
+                                            static_cast<const float*>(residual_in), T, d, k,
+                                            static_cast<float*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

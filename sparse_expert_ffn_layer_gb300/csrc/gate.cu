@@ -1,0 +1,166 @@
+// Gate: fp32 logits, softmax and top-k.
+//
+// Each token reaches its experts through a gating function (DeepSpeed-MoE review, "MoE based
+// NLG Model Architecture"); Top2-MoE sends it to two (same review, "Phenomenon2").  The
+// logits are the fp32 chain acc = fmaf(x[t,i], Wg[i,e], acc) for i ascending from +0: each
+// thread owns whole outputs of a register tile and walks the shared dimension in order, so
+// the result is bit-identical to any IEEE evaluation of that chain and routing is exact.
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTT = 64;   // tokens per block tile
+constexpr int kTE = 64;   // experts per block tile
+constexpr int kKC = 32;   // shared-dimension chunk staged in shared memory
+
+template <typename Tin>
+__device__ __forceinline__ float to_f32(Tin v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+
+// logits[T, E] = x[T, d] . Wg[d, E]; 256 threads, 4 x 4 outputs per thread.
+template <typename Tin>
+__global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict__ x,
+                                                          const float* __restrict__ Wg, int T,
+                                                          int d, int E,
+                                                          float* __restrict__ logits) {
+  __shared__ float xs[kTT][kKC + 1];             // x tile: xs[t][i], padded against conflicts
+  __shared__ __align__(16) float ws[kKC][kTE];   // Wg tile: ws[i][e]
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+
+  for (int k0 = 0; k0 < d; k0 += kKC) {
+    const int kc = min(kKC, d - k0);
+    // stage x[t0 .. t0+63][k0 .. k0+kc) and Wg[k0 .. k0+kc)[e0 .. e0+63]
+    for (int q = threadIdx.x; q < kTT * kKC; q += 256) {
+      int tt = q / kKC, kk = q % kKC;
+      int t = t0 + tt;
+      xs[tt][kk] = (t < T && kk < kc) ? to_f32<Tin>(x[(size_t)t * d + k0 + kk]) : 0.0f;
+    }
+    for (int q = threadIdx.x; q < kTE * kKC; q += 256) {
+      int kk = q / kTE, ee = q % kTE;
+      int e = e0 + ee;
+      ws[kk][ee] = (e < E && kk < kc) ? Wg[(size_t)(k0 + kk) * E + e] : 0.0f;
+    }
+    __syncthreads();
+    for (int kk = 0; kk < kc; ++kk) {            // ascending i, no padding steps
+      float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+      float av[4] = {xs[ty * 4][kk], xs[ty * 4 + 1][kk], xs[ty * 4 + 2][kk], xs[ty * 4 + 3][kk]};
+      float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int e = e0 + tx * 4 + j;
+      if (e < E) logits[(size_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+
+// (v, i) beats (w, j) when v > w, or v == w and i < j: descending logit, ties to lower index.
+__device__ __forceinline__ bool beats(float v, int i, float w, int j) {
+  return v > w || (v == w && i < j);
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    if (beats(v2, i2, v, i)) { v = v2; i = i2; }
+  }
+}
+
+// One warp per token: softmax over E (fp32) and top-k on the logits.
+__global__ void __launch_bounds__(256) softmax_topk_kernel(const float* __restrict__ logits, int T,
+                                                           int E, int k,
+                                                           float* __restrict__ probs_out,
+                                                           int32_t* __restrict__ topk_idx,
+                                                           float* __restrict__ topk_w,
+                                                           float* __restrict__ logits_copy) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* l = logits + (size_t)t * E;
+  float v1 = -INFINITY;
+  int i1 = 0x7fffffff;
+  for (int e = lane; e < E; e += 32) {
+    float v = l[e];
+    if (logits_copy) logits_copy[(size_t)t * E + e] = v;
+    if (beats(v, e, v1, i1)) { v1 = v; i1 = e; }
+  }
+  warp_argmax(v1, i1);
+  float v2 = -INFINITY;
+  int i2 = 0x7fffffff;
+  if (k == 2) {
+    for (int e = lane; e < E; e += 32) {
+      float v = l[e];
+      if (e != i1 && beats(v, e, v2, i2)) { v2 = v; i2 = e; }
+    }
+    warp_argmax(v2, i2);
+  }
+  float s = 0.0f;
+  for (int e = lane; e < E; e += 32) s += expf(l[e] - v1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (probs_out) {
+    float inv = 1.0f / s;
+    for (int e = lane; e < E; e += 32) probs_out[(size_t)t * E + e] = expf(l[e] - v1) * inv;
+  }
+  if (lane == 0) {
+    if (k == 1) {
+      topk_idx[t] = i1;
+      topk_w[t] = 1.0f / s;                         // p[e1] = exp(0) / sum
+    } else {
+      float r = expf(v2 - v1);                      // p2 / p1
+      float z = 1.0f + r;
+      topk_idx[2 * t] = i1;
+      topk_idx[2 * t + 1] = i2;
+      topk_w[2 * t] = 1.0f / z;
+      topk_w[2 * t + 1] = r / z;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, int T, int d, int E,
+                               float* logits, cudaStream_t s) {
+  dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);
+  if (dtype_f16)
+    gate_logits_kernel<__half><<<grid, 256, 0, s>>>(static_cast<const __half*>(x), Wg, T, d, E,
+                                                   logits);
+  else
+    gate_logits_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), Wg, T, d, E,
+                                                  logits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_topk(const float* logits, int T, int E, int k, float* probs_out,
+                                int32_t* topk_idx, float* topk_w, float* logits_copy,
+                                cudaStream_t s) {
+  const int warps = 8;
+  softmax_topk_kernel<<<(T + warps - 1) / warps, warps * 32, 0, s>>>(logits, T, E, k, probs_out,
+                                                                      topk_idx, topk_w,
+                                                                      logits_copy);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,387 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// Both GEMMs of the expert FFN run "swap-AB": the weight tile is the MMA's M = 128 operand
+// (A, read M-major straight from the row-major weights) and the tokens are the N operand
+// (B, K-major rows), so N is the ragged per-expert row count, rounded up to 16.
+//
+//   GEMM1  H[s, :]   = GeLU_tanh(X[perm[s], :] . W1[e])     A = W1[e]^T tile, B = gathered X rows
+//   GEMM2  out[t, :] (+)= w_s (H[s, :] . W2[e])              A = W2[e]^T tile, B = H rows
+//
+// Weight streaming dominates the bytes of the layer at every configured size: reading the
+// expert weights from memory is the bottleneck of MoE inference (DeepSpeed-MoE review,
+// "PR-MoE and MoS"), and small-batch GEMMs are bound by memory bandwidth (DeepSpeed
+// Inference review, "제안 방법").  So each (expert, M-tile) weight tile is read once, by one
+// CTA, through a deep TMA pipeline, while the token rows come from L2.
+//
+// Kernel shape: persistent, one CTA per SM, 6 warps.
+//   warp 0      producer: TMA of the A tile (two 64-wide boxes, 128-byte swizzle) and of the
+//               B rows (tile::gather4 through perm for GEMM1, 16-row boxes for GEMM2)
+//   warp 1      TMEM allocation and the MMA issue (one elected lane)
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, GeLU / gate-weighted combine,
+//               stores; TMEM double-buffered so the epilogue of tile i overlaps tile i+1.
+// Work items are (tile of <= nmax rows of one group, M-tile), groups being the experts in
+// slot order plus, for the residual variant, one group of all T tokens using the dense MLP
+// weights (PR-MoE's fixed MLP, DeepSpeed-MoE review "Phenomenon2": Residual-MoE).
+// Every wait is bounded: a stalled pipeline records MOE_ERR_TIMEOUT and the CTA leaves.
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;          // MMA M (weight rows per tile)
+constexpr int kBK = 64;           // K per pipeline stage (one 128-byte swizzle span of f16)
+constexpr int kABytes = kBM * kBK * 2;
+
+struct SmemLayout {
+  uint32_t stage_bytes, b_off, bars_off, misc_off, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int nmax, int stages, int E) {
+  SmemLayout L;
+  L.b_off = kABytes;
+  L.stage_bytes = kABytes + (uint32_t)nmax * 128u;
+  uint32_t off = (uint32_t)stages * L.stage_bytes;
+  L.bars_off = off;
+  off += (uint32_t)(2 * stages + 4) * 8u;
+  L.misc_off = off;
+  off += 16u + 4u * (uint32_t)(E + 1);       // tmem base, abort flag, chunk prefix
+  L.total = off + 1024u;                     // slack for 1024-byte alignment
+  return L;
+}
+
+struct Tile {
+  int res;      // 1: residual group
+  int e;        // expert (res == 0)
+  int row0;     // first row of the tile: slot (experts) or token (residual)
+  int n;        // valid rows
+  int mt;       // M-tile index
+  int K;        // shared dimension
+};
+
+// Maps work item i to its tile.  prefix[e] = chunks of experts < e (prefix[E] = total).
+__device__ __forceinline__ Tile decode(int i, const GemmArgs& a, const int32_t* prefix,
+                                       const int32_t* offs) {
+  Tile t;
+  const int n_exp = prefix[a.E] * a.mt_exp;
+  if (i < n_exp) {
+    const int j = i / a.mt_exp;
+    t.mt = i - j * a.mt_exp;
+    int lo = 0, hi = a.E;                   // largest e with prefix[e] <= j
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= j) lo = mid; else hi = mid;
+    }
+    t.res = 0;
+    t.e = lo;
+    const int chunk = j - prefix[lo];
+    const int kept = offs[lo + 1] - offs[lo];
+    t.row0 = offs[lo] + chunk * a.nmax;
+    t.n = min(a.nmax, kept - chunk * a.nmax);
+    t.K = a.K;
+  } else {
+    const int q = i - n_exp;
+    const int j = q / a.mt_res;
+    t.mt = q - j * a.mt_res;
+    t.res = 1;
+    t.e = 0;
+    t.row0 = j * a.nmax;
+    t.n = min(a.nmax, a.n_res_rows - t.row0);
+    t.K = a.K_res;
+  }
+  return t;
+}
+
+template <bool kGatherB, int kEpi>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmA_res,
+                        const __grid_constant__ CUtensorMap tmB_res, const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const SmemLayout L = smem_layout(a.nmax, a.stages, a.E);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off);
+  uint64_t* empty = full + a.stages;
+  uint64_t* acc_full = empty + a.stages;     // [2]
+  uint64_t* acc_empty = acc_full + 2;        // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.misc_off + 16);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (a.n_res_rows > 0) {
+      prefetch_tmap(&tmA_res);
+      prefetch_tmap(&tmB_res);
+    }
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 2 * a.acc_cols);
+  // chunk prefix over experts (warp 2), E <= 1024
+  if (warp == 2) {
+    const int per = (a.E + 31) / 32;
+    const int e_lo = lane * per, e_hi = min(a.E, e_lo + per);
+    int local = 0;
+    for (int e = e_lo; e < e_hi; ++e) {
+      const int kept = a.offsets[e + 1] - a.offsets[e];
+      local += (kept + a.nmax - 1) / a.nmax;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e_lo; e < e_hi; ++e) {
+      prefix[e] = run;
+      const int kept = a.offsets[e + 1] - a.offsets[e];
+      run += (kept + a.nmax - 1) / a.nmax;
+    }
+    if (lane == 31) prefix[a.E] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int n_exp_items = prefix[a.E] * a.mt_exp;
+  const int n_res_items = a.n_res_rows > 0 ? ((a.n_res_rows + a.nmax - 1) / a.nmax) * a.mt_res : 0;
+  const int total = n_exp_items + n_res_items;
+
+  uint32_t issued = 0, issued_parity = 0;     // producer: stages with a fill in flight
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x) {
+      const Tile t = decode(i, a, prefix, a.offsets);
+      const int npad = max(16, (t.n + 15) & ~15);
+      const CUtensorMap* mA = t.res ? &tmA_res : &tmA;
+      const CUtensorMap* mB = t.res ? &tmB_res : &tmB;
+      const int a_y0 = t.res ? 0 : t.e * a.a_rows_per_expert;
+      const int a_x = t.mt * kBM;
+      // this lane's gather rows (GEMM1): groups g = lane, lane + 32 of four rows each
+      int rows[2][4];
+      if (kGatherB) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            int r = 4 * (lane + 32 * h) + q;
+            int rr = r < t.n ? r : 0;
+            int src = t.row0 + rr;
+            rows[h][q] = t.res ? src : a.perm[src];
+          }
+      }
+      const int nkb = t.K / kBK;
+      for (int kb = 0; kb < nkb; ++kb) {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, a.wait_ns);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        uint8_t* sA = smem + (size_t)stage * L.stage_bytes;
+        uint8_t* sB = sA + L.b_off;
+        if (lane == 0) {
+          mbar_expect_tx(&full[stage], (uint32_t)kABytes + (uint32_t)npad * 128u);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tma_load_2d(sA, mA, a_x, a_y0 + kb * kBK, &full[stage]);
+          tma_load_2d(sA + kABytes / 2, mA, a_x + 64, a_y0 + kb * kBK, &full[stage]);
+        }
+        if (kGatherB) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int g = lane + 32 * h;
+            if (4 * g < npad)
+              tma_gather4(sB + g * 512, mB, kb * kBK, rows[h][0], rows[h][1], rows[h][2], rows[h][3],
+                          &full[stage]);
+          }
+        } else {
+          for (int b = lane; b < npad / 16; b += 32)
+            tma_load_2d(sB + b * 2048, mB, kb * kBK, t.row0 + 16 * b, &full[stage]);
+        }
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == a.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++local) {
+      const Tile t = decode(i, a, prefix, a.offsets);
+      const int npad = max(16, (t.n + 15) & ~15);
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1) & 1u;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_bounded(&acc_empty[buf], use ^ 1u, abort_flag, a.status, a.wait_ns);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)buf * a.acc_cols;
+      const uint32_t idesc = idesc_f16(kBM, npad, 1, 0);
+      const int nkb = t.K / kBK;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (lane == 0) ok = mbar_wait_bounded(&full[stage], phase, abort_flag, a.status, a.wait_ns);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(smem + (size_t)stage * L.stage_bytes);
+          const uint32_t b0 = a0 + L.b_off;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = smem_desc(a0 + kk * 2048, a.a_lbo, a.a_sbo, 2);
+            const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
+            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);        // frees the stage once these MMAs have read it
+        }
+        __syncwarp();
+        if (++stage == a.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&acc_full[buf]);
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
+    const int row_in_tile = 32 * quarter + lane;
+    if (kEpi == kEpiGeluH) {
+      // pre-work while the first tiles stream in: zero buffers the next kernel accumulates into
+      const int ep_tid = blockIdx.x * 128 + (threadIdx.x - 64);
+      const int ep_threads = gridDim.x * 128;
+      if (a.zero_f32) {
+        float4* z4 = reinterpret_cast<float4*>(a.zero_f32);
+        const size_t n4 = a.zero_f32_n / 4;
+        for (size_t q = ep_tid; q < n4; q += ep_threads) z4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (a.drop_out) {
+        const int gw = ep_tid >> 5, nw = ep_threads >> 5;
+        for (int tok = gw; tok < a.drop_T; tok += nw) {
+          if (a.drop_slot_of[tok] >= 0) continue;
+          uint4* row = reinterpret_cast<uint4*>(a.drop_out + (size_t)tok * a.drop_d);
+          for (int c = lane; c < a.drop_d / 8; c += 32) row[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
+    int local = 0;
+    for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++local) {
+      const Tile t = decode(i, a, prefix, a.offsets);
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1) & 1u;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_bounded(&acc_full[buf], use, abort_flag, a.status, a.wait_ns);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const int m = t.mt * kBM + row_in_tile;
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)buf * a.acc_cols;
+      for (int c0 = 0; c0 < t.n; c0 += 16) {
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int s = c0 + j;
+          if (s >= t.n) break;
+          const int row = t.row0 + s;
+          if (kEpi == kEpiGeluH) {
+            const __half h = __float2half_rn(gelu_tanh(v[j]));
+            if (t.res) a.hres_out[(size_t)row * a.ldhres + m] = h;
+            else a.h_out[(size_t)row * a.ldh + m] = h;
+          } else {
+            if (t.res) {
+              a.r32[(size_t)row * a.ldo + m] = v[j];
+            } else if (a.mode == kModeExpertOut) {
+              a.out[(size_t)row * a.ldo + m] = __float2half_rn(v[j]);
+            } else {
+              const int tok = a.perm[row];
+              const float w = a.slot_w[row];
+              if (a.mode == kModeDirect) a.out[(size_t)tok * a.ldo + m] = __float2half_rn(w * v[j]);
+              else red_add_f32(a.acc32 + (size_t)tok * a.ldo + m, w * v[j]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // let the last copy issued into each stage land before the CTA's shared memory is
+    // released (bounded: 100 ms per stage)
+    for (int s = 0; s < a.stages; ++s) {
+      if (!(issued >> s & 1u)) continue;
+      const uint32_t par = issued_parity >> s & 1u;
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&full[s], par)) {
+        if (globaltimer_ns() - t0 > 100000000ull) break;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, 2 * a.acc_cols);
+}
+
+template <bool G, int Epi>
+cudaError_t launch_one(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
+                       const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s) {
+  const SmemLayout L = smem_layout(args.nmax, args.stages, args.E);
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<G, Epi>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+  if (err != cudaSuccess) return err;
+  grouped_gemm_kernel<G, Epi><<<grid, kThreads, L.total, s>>>(A, B, Ar, Br, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_stages_for(int nmax, int E, int smem_limit) {
+  for (int st = 8; st >= 2; --st)
+    if ((int)smem_layout(nmax, st, E).total <= smem_limit) return st;
+  return 0;
+}
+
+cudaError_t launch_grouped_gemm1(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
+                                 const CUtensorMap& Br, const GemmArgs& args, int grid,
+                                 cudaStream_t s) {
+  return launch_one<true, kEpiGeluH>(A, B, Ar, Br, args, grid, s);
+}
+
+cudaError_t launch_grouped_gemm2(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
+                                 const CUtensorMap& Br, const GemmArgs& args, int grid,
+                                 cudaStream_t s) {
+  return launch_one<false, kEpiCombine>(A, B, Ar, Br, args, grid, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,104 @@
+// Internal interface between the C-ABI front end (api.cu) and the kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// Epilogue kinds of the grouped GEMM.
+enum : int { kEpiGeluH = 0, kEpiCombine = 1 };
+// Output modes of the second GEMM's epilogue (expert tiles).
+enum : int {
+  kModeDirect = 0,     // out[perm[s]] = f16(w_s * acc): top-1, no residual; each token once
+  kModeAccum = 1,      // acc32[perm[s]] += w_s * acc (fp32 reduction, <= 2 addends per element)
+  kModeExpertOut = 2   // out[s] = f16(acc): unscaled rows in slot order (moe_expert_ffn)
+};
+
+struct GemmArgs {
+  // groups
+  const int32_t* offsets;   // [E + 1] slot offsets per expert
+  const int32_t* perm;      // [S] token of each slot
+  int E;
+  int n_res_rows;           // rows of the residual group (T), 0 when absent
+  int K, K_res;             // shared dimension of expert / residual tiles
+  int mt_exp, mt_res;       // M-tiles (of 128) per expert / residual tile
+  int a_rows_per_expert;    // rows of the A tensor map per expert
+  int nmax;                 // rows per tile, multiple of 16, <= 256
+  int stages;               // pipeline depth
+  uint32_t acc_cols;        // TMEM columns per accumulator buffer (power of two >= 32)
+  uint32_t a_lbo, a_sbo;    // A (M-major, 128-byte swizzle) descriptor byte offsets
+  int mode;                 // kMode* (second GEMM)
+  // first GEMM outputs
+  __half* h_out;            // [S_max, ldh]
+  int ldh;
+  __half* hres_out;         // [T, ldhres]
+  int ldhres;
+  // second GEMM outputs
+  __half* out;              // kModeDirect: [T, ldo]; kModeExpertOut: [S_max, ldo]
+  float* acc32;             // kModeAccum: [T, ldo]
+  float* r32;               // residual tiles: [T, ldo]
+  int ldo;
+  const float* slot_w;      // [S] gate weight of each slot
+  // first GEMM pre-work (epilogue warps, before the first tile)
+  float* zero_f32;          // buffer to clear, or null
+  size_t zero_f32_n;        // its length in floats (multiple of 4)
+  const int32_t* drop_slot_of;  // [T] slot of each token (top-1) for zeroing dropped rows
+  int drop_T;
+  __half* drop_out;         // out [T, drop_d], or null
+  int drop_d;
+  // error reporting
+  int* status;
+  uint64_t wait_ns;
+};
+
+cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, int T, int d, int E,
+                               float* logits, cudaStream_t s);
+cudaError_t launch_softmax_topk(const float* logits, int T, int E, int k, float* probs_out,
+                                int32_t* topk_idx, float* topk_w, float* logits_copy,
+                                cudaStream_t s);
+size_t dispatch_smem_bytes(int E);
+cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C,
+                            int32_t* counts_raw, int32_t* kept, int32_t* offsets, int32_t* perm,
+                            int32_t* slot_of, const float* topk_w, float* slot_w, cudaStream_t s);
+
+int gemm_stages_for(int nmax, int E, int smem_limit);
+cudaError_t launch_grouped_gemm1(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
+                                 const CUtensorMap& Br, const GemmArgs& args, int grid,
+                                 cudaStream_t s);
+cudaError_t launch_grouped_gemm2(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
+                                 const CUtensorMap& Br, const GemmArgs& args, int grid,
+                                 cudaStream_t s);
+
+// fp32 SIMT path (small layers)
+struct SimtArgs {
+  const float* x;           // [T, d]
+  const int32_t* offsets;   // [E + 1]
+  const int32_t* perm;      // [S]
+  const float* W1;          // [E, d, f]
+  const float* W2;          // [E, f, d]
+  const float* Wr1;         // [d, f_res] or null
+  const float* Wr2;         // [f_res, d]
+  int T, d, f, E, f_res;
+  float* H;                 // [S_max, f]
+  float* Hres;              // [T, f_res]
+  int mode;                 // kMode*
+  float* out;               // kModeDirect: [T, d]; kModeExpertOut: [S_max, d]
+  float* acc32;             // kModeAccum: [T, d]
+  float* r32;               // residual: [T, d]
+  const float* slot_w;
+};
+cudaError_t launch_simt_ffn1(const SimtArgs& a, int S_max, cudaStream_t s);
+cudaError_t launch_simt_ffn2(const SimtArgs& a, int S_max, cudaStream_t s);
+
+// elementwise kernels
+cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
+cudaError_t launch_zero_dropped_rows(const int32_t* slot_of, int T, int k, int d, int dtype_f16,
+                                     void* out, cudaStream_t s);
+cudaError_t launch_finalize(const float* acc32, const float* r32, int T, int d, int dtype_f16,
+                            void* out, cudaStream_t s);
+cudaError_t launch_combine(const void* expert_out, const int32_t* slot_of, const float* topk_w,
+                           const void* residual_in, int dtype_f16, int T, int d, int k, void* out,
+                           cudaStream_t s);
+cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace moe
