@@ -198,6 +198,20 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------ ranks
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank timings (the slowest rank defines the job's time)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(world, T, K, ms):
+    """Whole-job throughput: every rank processed K steps of T tokens in at most `ms`."""
+    return world * T * K / (ms / 1000.0)
+
+
 # ------------------------------------------------------------------------ GPU arm
 def traffic_record(kernel_file):
     """Per-launch DRAM bytes from the committed ncu summary, if taken on this kernel source."""
@@ -325,15 +339,13 @@ def run_ours(args):
     ms_e2e = h0.elapsed_time(h1)
 
     if world > 1:
-        t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+        ms, ms_e2e = max_over_ranks([ms, ms_e2e], dist, "cuda")
     if rank != 0:
         dist.destroy_process_group()
         return
 
-    value = world * T * K / (ms / 1000.0)
-    value_e2e = world * T * K / (ms_e2e / 1000.0)
+    value = job_tokens_per_s(world, T, K, ms)
+    value_e2e = job_tokens_per_s(world, T, K, ms_e2e)
     hbm, bf16, bf16_sus, peak_src = peaks()
     el = 2 if f16 else 4
     # algorithmic bytes per launch: the active experts' weights once, plus activations

@@ -25,9 +25,14 @@ int capacity_of(int T, int E, float cf) {
 }
 
 // ---------------------------------------------------------------- workspace layout
+// Split-K applies to decode-sized batches only: at most kMaxSplit chunks, and only when the
+// expert slots plus residual rows fit in kSplitRows (the fp32 partial sums then stay small).
+constexpr int kMaxSplit = 32;
+constexpr int kSplitRows = 64;
+
 struct Ws {
   size_t status, logits, topk_idx, topk_w, counts, kept, offsets, perm, slot_w, slot_of, H, Hres,
-      acc32, r32, total;
+      acc32, r32, partial, partial_bytes, total;
 };
 
 Ws ws_layout(int T, int d, int f, int E, int k, int C, bool residual, int f_res, bool f16) {
@@ -55,6 +60,14 @@ Ws ws_layout(int T, int d, int f, int E, int k, int C, bool residual, int f_res,
   w.Hres = residual ? take((size_t)T * f_res * elt) : 0;
   w.acc32 = accum ? take((size_t)T * d * 4) : 0;
   w.r32 = residual ? take((size_t)T * d * 4) : 0;
+  const size_t part_rows = S_max + (residual ? (size_t)T : 0);
+  w.partial_bytes = 0;
+  w.partial = 0;
+  if (f16 && part_rows <= (size_t)kSplitRows) {
+    const size_t cols = std::max<size_t>(std::max(f, d), residual ? f_res : 0);
+    w.partial_bytes = (size_t)kMaxSplit * part_rows * cols * 4;
+    w.partial = take(w.partial_bytes);
+  }
   w.total = off;
   return w;
 }
@@ -155,6 +168,14 @@ bool tc_plan(int rows_bound, int E, TcPlan* p) {
   return p->stages >= 2;
 }
 
+// Chunks per tile so that a launch has about four waves of work items, each chunk keeping at
+// least two 64-wide K blocks.
+int choose_ksplit(long long items_bound, int nkb_min, int sms) {
+  int ks = 1;
+  while (ks * 2 <= kMaxSplit && items_bound * ks < 4LL * sms && nkb_min / (ks * 2) >= 2) ks *= 2;
+  return ks;
+}
+
 // A (M-major weights) descriptor offsets for the 128-byte swizzle layout that two 64-wide
 // TMA boxes of 64 K-rows produce: M-blocks 8 KB apart, 8-row K groups 1 KB apart.
 constexpr uint32_t kALbo = 8192, kASbo = 1024;
@@ -169,6 +190,7 @@ void fill_common(GemmArgs& g, const TcPlan& p, int E, int* status) {
   g.a_sbo = kASbo;
   g.status = status;
   g.wait_ns = kDefaultWaitNs;
+  g.ksplit = 1;
 }
 
 thread_local cudaEvent_t* t_stage_events = nullptr;
@@ -189,11 +211,25 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
                       const void* W1, const void* W2, const void* Wr1, const void* Wr2, int T,
                       int d, int f, int E, int f_res, int S_rows, int rows_bound, __half* H,
                       __half* Hres, int mode, void* out, float* acc32, float* r32,
-                      const float* slot_w, const int32_t* drop_slot_of, int* status,
-                      cudaStream_t s) {
+                      const float* slot_w, const int32_t* drop_slot_of, float* partial,
+                      size_t partial_bytes, int* status, cudaStream_t s) {
   const bool residual = Wr1 != nullptr;
   TcPlan plan;
   if (!tc_plan(rows_bound, E, &plan)) return MOE_ERR_CUDA;
+  const int T_res = residual ? T : 0;
+  const int part_rows = S_rows + T_res;
+  const long long tiles_bound = std::min(E, S_rows) + S_rows / plan.nmax;
+  const long long res_tiles = residual ? (T + plan.nmax - 1) / plan.nmax : 0;
+  int ks1 = 1, ks2 = 1;
+  if (partial) {
+    ks1 = choose_ksplit(tiles_bound * (f / 128) + res_tiles * (residual ? f_res / 128 : 0), d / 64,
+                        plan.grid);
+    ks2 = choose_ksplit((tiles_bound + res_tiles) * (d / 128),
+                        residual ? std::min(f, f_res) / 64 : f / 64, plan.grid);
+    const size_t cols1 = std::max(f, residual ? f_res : 0);
+    if ((size_t)ks1 * part_rows * cols1 * 4 > partial_bytes) ks1 = 1;
+    if ((size_t)ks2 * part_rows * d * 4 > partial_bytes) ks2 = 1;
+  }
   CUtensorMap mW1, mX, mWr1, mW2, mH, mWr2, mHres;
   const int S_dim = std::max(S_rows, 1);
   if (!make_map(&mW1, W1, f, (uint64_t)E * d, 64, 64) || !make_map(&mX, tokens, d, T, 64, 1) ||
@@ -232,7 +268,13 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
     g1.drop_out = static_cast<__half*>(out);
     g1.drop_d = d;
   }
+  g1.ksplit = ks1;
+  g1.partial = partial;
+  g1.part_rows = part_rows;
+  g1.part_cols = std::max(f, residual ? f_res : 0);
+  g1.part_res_row0 = S_rows;
   MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan.grid, s));
+  if (ks1 > 1) MOE_TRY(launch_splitk_reduce1(g1, S_rows, T_res, f, f_res, s));
   MOE_TRY(stage_mark(4, s));
 
   GemmArgs g2;
@@ -251,7 +293,13 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   g2.r32 = r32;
   g2.ldo = d;
   g2.slot_w = slot_w;
+  g2.ksplit = ks2;
+  g2.partial = partial;
+  g2.part_rows = part_rows;
+  g2.part_cols = d;
+  g2.part_res_row0 = S_rows;
   MOE_TRY(launch_grouped_gemm2(mW2, mH, mWr2, mHres, g2, plan.grid, s));
+  if (ks2 > 1) MOE_TRY(launch_splitk_reduce2(g2, S_rows, T_res, d, s));
   MOE_TRY(stage_mark(5, s));
   return MOE_OK;
 }
@@ -335,7 +383,7 @@ moe_status moe_expert_ffn(const void* tokens, const int32_t* perm, const int32_t
   if (f16) {
     return run_tc_ffn(tokens, perm, offsets, W1, W2, nullptr, nullptr, T, d, f, E, 0, S_max, S_max,
                       reinterpret_cast<__half*>(ws + kAlign), nullptr, kModeExpertOut, expert_out,
-                      nullptr, nullptr, nullptr, nullptr, status, s);
+                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, s);
   }
   SimtArgs a;
   memset(&a, 0, sizeof(a));
@@ -421,7 +469,9 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
                     T, d, f, E, residual ? f_res : 0, S_max, rows_bound,
                     reinterpret_cast<__half*>(ws + L.H),
                     residual ? reinterpret_cast<__half*>(ws + L.Hres) : nullptr, mode, out, acc32, r32,
-                    slot_w, k == 1 ? slot_of : nullptr, status, s);
+                    slot_w, k == 1 ? slot_of : nullptr,
+                    L.partial_bytes ? reinterpret_cast<float*>(ws + L.partial) : nullptr,
+                    L.partial_bytes, status, s);
     if (st != MOE_OK) return st;
   } else {
     SimtArgs a;

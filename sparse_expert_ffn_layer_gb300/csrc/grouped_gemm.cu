@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_exp_items = prefix[a.E] * a.mt_exp;
   const int n_res_items = a.n_res_rows > 0 ? ((a.n_res_rows + a.nmax - 1) / a.nmax) * a.mt_res : 0;
-  const int total = n_exp_items + n_res_items;
+  const int ksplit = a.ksplit;
+  const int total = (n_exp_items + n_res_items) * ksplit;
 
   uint32_t issued = 0, issued_parity = 0;     // producer: stages with a fill in flight
   if (warp == 0) {
@@ -170,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x) {
-      const Tile t = decode(i, a, prefix, a.offsets);
+      const Tile t = decode(i / ksplit, a, prefix, a.offsets);
+      const int ks = i - (i / ksplit) * ksplit;
       const int npad = max(16, (t.n + 15) & ~15);
       const CUtensorMap* mA = t.res ? &tmA_res : &tmA;
       const CUtensorMap* mB = t.res ? &tmB_res : &tmB;
@@ -190,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
       }
       const int nkb = t.K / kBK;
-      for (int kb = 0; kb < nkb; ++kb) {
+      const int kb0 = ks * nkb / ksplit, kb1 = (ks + 1) * nkb / ksplit;
+      for (int kb = kb0; kb < kb1; ++kb) {
         bool ok = true;
         if (lane == 0) ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, a.wait_ns);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -231,7 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int local = 0;
     for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++local) {
-      const Tile t = decode(i, a, prefix, a.offsets);
+      const Tile t = decode(i / ksplit, a, prefix, a.offsets);
+      const int ks = i - (i / ksplit) * ksplit;
       const int npad = max(16, (t.n + 15) & ~15);
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1) & 1u;
@@ -243,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d_tmem = tmem_base + (uint32_t)buf * a.acc_cols;
       const uint32_t idesc = idesc_f16(kBM, npad, 1, 0);
       const int nkb = t.K / kBK;
-      for (int kb = 0; kb < nkb; ++kb) {
+      const int kb0 = ks * nkb / ksplit, kb1 = (ks + 1) * nkb / ksplit;
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (lane == 0) ok = mbar_wait_bounded(&full[stage], phase, abort_flag, a.status, a.wait_ns);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = smem_desc(a0 + kk * 2048, a.a_lbo, a.a_sbo, 2);
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
-            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_f16(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
           }
           tc_commit(&empty[stage]);        // frees the stage once these MMAs have read it
         }
@@ -293,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int local = 0;
     for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++local) {
-      const Tile t = decode(i, a, prefix, a.offsets);
+      const Tile t = decode(i / ksplit, a, prefix, a.offsets);
+      const int ks = i - (i / ksplit) * ksplit;
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1) & 1u;
       bool ok = true;
@@ -311,7 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = c0 + j;
           if (s >= t.n) break;
           const int row = t.row0 + s;
-          if (kEpi == kEpiGeluH) {
+          if (ksplit > 1) {
+            const int prow = t.res ? a.part_res_row0 + row : row;
+            a.partial[((size_t)ks * a.part_rows + prow) * a.part_cols + m] = v[j];
+          } else if (kEpi == kEpiGeluH) {
             const __half h = __float2half_rn(gelu_tanh(v[j]));
             if (t.res) a.hres_out[(size_t)row * a.ldhres + m] = h;
             else a.h_out[(size_t)row * a.ldh + m] = h;
