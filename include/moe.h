@@ -108,7 +108,8 @@ MOE_API moe_status moe_gate_topk(const void* tokens, moe_dtype dtype, const floa
 
 /*
  * Capacity-limited dispatch (reading: token-major order, capacity ceil(cf T / E)).
- *   topk_idx   [T, k] int32 experts (values outside [0, E) are out of contract).
+ *   topk_idx   [T, k] int32 experts; an index outside [0, E) is not counted and its
+ *              assignment is dropped (slot_of = -1).
  *   counts_raw [E]    assignments per expert before the capacity cut.
  *   kept       [E]    min(counts_raw, C).
  *   offsets    [E+1]  exclusive scan of kept; offsets[E] = S, the number of kept slots.

@@ -331,12 +331,12 @@ moe_status moe_gate_topk(const void* tokens, moe_dtype dtype, const float* Wg,
                          float* probs_out, int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
   if (T < 0 || d < 1 || E < 1 || (k != 1 && k != 2) || k > E) return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_F16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
-  if (!topk_idx || !topk_w || (!logits_in && (!tokens || !Wg))) return MOE_ERR_INVALID_ARG;
   if (E > kMaxE || (long long)T * E > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;                       // empty batch: nothing to read or write
+  if (!topk_idx || !topk_w || (!logits_in && (!tokens || !Wg))) return MOE_ERR_INVALID_ARG;
   if (!aligned16(tokens) || !aligned16(Wg) || !aligned16(logits_in) || !aligned16(logits_out) ||
       !aligned16(probs_out) || !aligned16(topk_idx) || !aligned16(topk_w))
     return MOE_ERR_UNSUPPORTED;
-  if (T == 0) return MOE_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (logits_in) {
     MOE_TRY(launch_softmax_topk(logits_in, T, E, k, probs_out, topk_idx, topk_w, logits_out, s));
@@ -354,9 +354,9 @@ moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k, float capa
   if (T < 0 || E < 1 || (k != 1 && k != 2) || k > E) return MOE_ERR_INVALID_ARG;
   const int C = capacity_of(T, E, capacity_factor);
   if (C < 0) return MOE_ERR_INVALID_ARG;
-  if (!topk_idx || !counts_raw || !kept || !offsets || !perm || !slot_of) return MOE_ERR_INVALID_ARG;
   if (E > kMaxE || (long long)T * k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
+  if (!topk_idx || !counts_raw || !kept || !offsets || !perm || !slot_of) return MOE_ERR_INVALID_ARG;
   MOE_TRY(launch_dispatch(topk_idx, T, k, E, C, counts_raw, kept, offsets, perm, slot_of, nullptr,
                           nullptr, reinterpret_cast<cudaStream_t>(stream)));
   return MOE_OK;
@@ -369,11 +369,11 @@ moe_status moe_expert_ffn(const void* tokens, const int32_t* perm, const int32_t
   moe_status st = check_shape(T, d, f, E, 1, dtype);
   if (st != MOE_OK) return st;
   if (S_max < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0 || S_max == 0) return MOE_OK;
   if (!tokens || !perm || !offsets || !W1 || !W2 || !expert_out) return MOE_ERR_INVALID_ARG;
   if (!aligned16(tokens) || !aligned16(W1) || !aligned16(W2) || !aligned16(expert_out) ||
       !aligned16(workspace))
     return MOE_ERR_UNSUPPORTED;
-  if (T == 0 || S_max == 0) return MOE_OK;
   const bool f16 = dtype == MOE_F16;
   if (!workspace || ws_bytes < expert_ffn_ws_bytes(S_max, f, f16)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -406,8 +406,8 @@ moe_status moe_combine(const void* expert_out, const int32_t* slot_of, const flo
                        moe_stream_t stream) {
   if (T < 0 || d < 1 || (k != 1 && k != 2)) return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_F16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
-  if (!expert_out || !slot_of || !topk_w || !out) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
+  if (!expert_out || !slot_of || !topk_w || !out) return MOE_ERR_INVALID_ARG;
   MOE_TRY(launch_combine(expert_out, slot_of, topk_w, residual_in, dtype == MOE_F16, T, d, k, out,
                          reinterpret_cast<cudaStream_t>(stream)));
   return MOE_OK;
@@ -424,15 +424,16 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
   const bool residual = mlp_type == MOE_MLP_RESIDUAL;
   const int C = capacity_of(T, E, capacity_factor);
   if (C < 0) return MOE_ERR_INVALID_ARG;
-  if (!tokens || !Wg || !W1 || !W2 || !out) return MOE_ERR_INVALID_ARG;
-  if (residual && (!Wr1 || !Wr2 || f_res < 1)) return MOE_ERR_INVALID_ARG;
+  if (residual && f_res < 1) return MOE_ERR_INVALID_ARG;
   if (residual && ((dtype == MOE_F16 && f_res % 128) || (dtype == MOE_F32 && f_res % 4)))
     return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;                       // empty batch: nothing to read or write
+  if (!tokens || !Wg || !W1 || !W2 || !out) return MOE_ERR_INVALID_ARG;
+  if (residual && (!Wr1 || !Wr2)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(tokens) || !aligned16(Wg) || !aligned16(W1) || !aligned16(W2) || !aligned16(out) ||
       !aligned16(workspace) || !aligned16(topk_idx_out) || !aligned16(slot_of_out) ||
       (residual && (!aligned16(Wr1) || !aligned16(Wr2))))
     return MOE_ERR_UNSUPPORTED;
-  if (T == 0) return MOE_OK;
   const bool f16 = dtype == MOE_F16;
   const Ws L = ws_layout(T, d, f, E, k, C, residual, residual ? f_res : 0, f16);
   if (!workspace || ws_bytes < L.total) return MOE_ERR_WORKSPACE;

@@ -42,8 +42,9 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
   // pass 1: rank inside the warp's run; kept temporarily in slot_of
   for (int base = a_begin; base < a_end; base += 32) {
     const int a = base + lane;
-    const bool valid = a < a_end;
-    const int e = valid ? topk_idx[a] : -1 - lane;     // invalid lanes form singleton groups
+    int e = a < a_end ? topk_idx[a] : -1;
+    const bool valid = (unsigned)e < (unsigned)E;      // out-of-range experts are dropped
+    if (!valid) e = -1 - lane;                         // invalid lanes form singleton groups
     const unsigned grp = __match_any_sync(0xffffffffu, e);
     const int leader = __ffs(grp) - 1;
     int before = 0;
@@ -105,6 +106,10 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
   // pass 3: global rank -> slot
   for (int a = a_begin + lane; a < a_end; a += 32) {
     const int e = topk_idx[a];
+    if ((unsigned)e >= (unsigned)E) {
+      slot_of[a] = -1;
+      continue;
+    }
     const int r = cnt[w * E + e] + slot_of[a];
     if (r < C) {
       const int s = offs[e] + r;
