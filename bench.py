@@ -294,8 +294,14 @@ def run_ours(args):
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_STAGE_EVENTS)]
            for _ in range(K)]
+    for ev_step in evs:                  # torch creates the CUDA event at its first record
+        for ev in ev_step:
+            ev.record(stream)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    props = torch.cuda.get_device_properties(local)
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else uuid
+    clocks = ClockSampler(gpu_id if gpu_id else str(local))
     clocks.start()
     time.sleep(0.3)
     if world > 1:

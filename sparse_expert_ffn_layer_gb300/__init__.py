@@ -176,5 +176,8 @@ def moe_set_stage_events(events=None):
     if events is None:
         _check(get_lib().moe_set_stage_events(None, 0), "moe_set_stage_events")
         return
-    arr = (ctypes.c_void_p * MOE_STAGE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    handles = [e.cuda_event for e in events]
+    if len(handles) != MOE_STAGE_EVENTS or not all(handles):
+        raise ValueError("moe_set_stage_events needs 7 created events (record each once first)")
+    arr = (ctypes.c_void_p * MOE_STAGE_EVENTS)(*[ctypes.c_void_p(h) for h in handles])
     _check(get_lib().moe_set_stage_events(arr, MOE_STAGE_EVENTS), "moe_set_stage_events")
