@@ -21,6 +21,7 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 32;
+constexpr int kUnroll = 8;      // batches of 32 assignments whose loads are issued together
 
 __global__ void __launch_bounds__(1024) dispatch_kernel(
     const int32_t* __restrict__ topk_idx, int n, int k, int E, int C,
@@ -39,22 +40,33 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
   const int a_begin = min(n, w * L), a_end = min(n, a_begin + L);
   const unsigned lt_mask = (1u << lane) - 1u;
 
-  // pass 1: rank inside the warp's run; kept temporarily in slot_of
-  for (int base = a_begin; base < a_end; base += 32) {
-    const int a = base + lane;
-    int e = a < a_end ? topk_idx[a] : -1;
-    const bool valid = (unsigned)e < (unsigned)E;      // out-of-range experts are dropped
-    if (!valid) e = -1 - lane;                         // invalid lanes form singleton groups
-    const unsigned grp = __match_any_sync(0xffffffffu, e);
-    const int leader = __ffs(grp) - 1;
-    int before = 0;
-    if (valid) before = cnt[w * E + e];
-    __syncwarp();
-    if (valid) {
-      slot_of[a] = before + __popc(grp & lt_mask);
-      if (lane == leader) cnt[w * E + e] = before + __popc(grp);
+  // pass 1: rank inside the warp's run; kept temporarily in slot_of.  Eight batches of 32
+  // assignments are fetched at once so their loads overlap.
+  for (int base = a_begin; base < a_end; base += 32 * kUnroll) {
+    int ev[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int a = base + 32 * u + lane;
+      ev[u] = a < a_end ? topk_idx[a] : -1;
     }
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (base + 32 * u >= a_end) break;                 // warp-uniform
+      const int a = base + 32 * u + lane;
+      int e = ev[u];
+      const bool valid = a < a_end && (unsigned)e < (unsigned)E;   // out-of-range: dropped
+      if (!valid) e = -1 - lane;                         // invalid lanes form singleton groups
+      const unsigned grp = __match_any_sync(0xffffffffu, e);
+      const int leader = __ffs(grp) - 1;
+      int before = 0;
+      if (valid) before = cnt[w * E + e];
+      __syncwarp();
+      if (valid) {
+        slot_of[a] = before + __popc(grp & lt_mask);
+        if (lane == leader) cnt[w * E + e] = before + __popc(grp);
+      }
+      __syncwarp();
+    }
   }
   __syncthreads();
 
@@ -103,21 +115,33 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
   }
   __syncthreads();
 
-  // pass 3: global rank -> slot
-  for (int a = a_begin + lane; a < a_end; a += 32) {
-    const int e = topk_idx[a];
-    if ((unsigned)e >= (unsigned)E) {
-      slot_of[a] = -1;
-      continue;
+  // pass 3: global rank -> slot (again eight batches of loads in flight)
+  for (int base = a_begin; base < a_end; base += 32 * kUnroll) {
+    int ev[kUnroll], rv[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int a = base + 32 * u + lane;
+      ev[u] = a < a_end ? topk_idx[a] : -1;
+      rv[u] = a < a_end ? slot_of[a] : 0;
     }
-    const int r = cnt[w * E + e] + slot_of[a];
-    if (r < C) {
-      const int s = offs[e] + r;
-      slot_of[a] = s;
-      perm[s] = a / k;
-      if (slot_w) slot_w[s] = topk_w[a];
-    } else {
-      slot_of[a] = -1;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int a = base + 32 * u + lane;
+      if (a >= a_end) continue;
+      const int e = ev[u];
+      if ((unsigned)e >= (unsigned)E) {
+        slot_of[a] = -1;
+        continue;
+      }
+      const int r = cnt[w * E + e] + rv[u];
+      if (r < C) {
+        const int s = offs[e] + r;
+        slot_of[a] = s;
+        perm[s] = a / k;
+        if (slot_w) slot_w[s] = topk_w[a];
+      } else {
+        slot_of[a] = -1;
+      }
     }
   }
 }

@@ -13,6 +13,119 @@ namespace {
 constexpr int kTT = 64;   // tokens per block tile
 constexpr int kTE = 64;   // experts per block tile
 constexpr int kKC = 32;   // shared-dimension chunk staged in shared memory
+constexpr int kXP = kKC + 4;  // padded row of the token tile (16-byte aligned rows)
+
+template <typename Tin>
+struct XChunk;  // one thread's share of a 64 x 32 token chunk: 8 consecutive values of a row
+
+template <>
+struct XChunk<__half> {
+  uint4 raw;
+  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void zero() { raw = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
+    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float2 f = __half22float2(h[q]);      // exact widening
+      v[2 * q] = f.x;
+      v[2 * q + 1] = f.y;
+    }
+  }
+};
+
+template <>
+struct XChunk<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 4);
+  }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+// logits[T, E] = x[T, d] . Wg[d, E]; 256 threads, 4 x 4 outputs per thread.  The next chunk
+// is fetched into registers while the current one is multiplied (double-buffered tiles).
+// Vector path: d % 8 == 0 and E % 4 == 0 (16-byte loads); otherwise the scalar kernel below.
+template <typename Tin>
+__global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict__ x,
+                                                          const float* __restrict__ Wg, int T,
+                                                          int d, int E,
+                                                          float* __restrict__ logits) {
+  __shared__ __align__(16) float xs[2][kTT][kXP];   // token tile: xs[t][i]
+  __shared__ __align__(16) float ws[2][kKC][kTE];   // Wg tile: ws[i][e]
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
+  // loader roles: token row lt, columns lk .. lk+7; Wg rows lw, lw+16 (4 experts at le)
+  const int lt = threadIdx.x >> 2, lk = (threadIdx.x & 3) * 8;
+  const int lw = threadIdx.x >> 4, le = (threadIdx.x & 15) * 4;
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+
+  XChunk<Tin> xr;
+  float4 wr0, wr1;
+  auto fetch = [&](int k0) {
+    const int t = t0 + lt;
+    const int kc = min(kKC, d - k0);
+    if (t < T && lk < kc) xr.load(x + (size_t)t * d + k0 + lk);
+    else xr.zero();
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool eok = e0 + le < E;
+    wr0 = (eok && lw < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw) * E + e0 + le) : z;
+    wr1 = (eok && lw + 16 < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw + 16) * E + e0 + le) : z;
+  };
+  auto stash = [&](int buf) {
+    float v[8];
+    xr.to_f32(v);
+    *reinterpret_cast<float4*>(&xs[buf][lt][lk]) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(&xs[buf][lt][lk + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+    *reinterpret_cast<float4*>(&ws[buf][lw][le]) = wr0;
+    *reinterpret_cast<float4*>(&ws[buf][lw + 16][le]) = wr1;
+  };
+
+  fetch(0);
+  stash(0);
+  __syncthreads();
+  int buf = 0;
+  for (int k0 = 0; k0 < d; k0 += kKC) {
+    const int kc = min(kKC, d - k0);
+    const bool more = k0 + kKC < d;
+    if (more) fetch(k0 + kKC);
+    for (int kk = 0; kk < kc; ++kk) {            // ascending i, no padding steps
+      const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][tx * 4]);
+      const float av[4] = {xs[buf][ty * 4][kk], xs[buf][ty * 4 + 1][kk], xs[buf][ty * 4 + 2][kk],
+                           xs[buf][ty * 4 + 3][kk]};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+    }
+    if (more) stash(buf ^ 1);
+    __syncthreads();
+    buf ^= 1;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+    const int e = e0 + tx * 4;
+    if (e + 3 < E) {
+      *reinterpret_cast<float4*>(logits + (size_t)t * E + e) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (e + j < E) logits[(size_t)t * E + e + j] = acc[i][j];
+    }
+  }
+}
 
 template <typename Tin>
 __device__ __forceinline__ float to_f32(Tin v);
@@ -21,14 +134,14 @@ __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
 
-// logits[T, E] = x[T, d] . Wg[d, E]; 256 threads, 4 x 4 outputs per thread.
+// Any d and E: scalar staging, same per-output chain.
 template <typename Tin>
-__global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict__ x,
-                                                          const float* __restrict__ Wg, int T,
-                                                          int d, int E,
-                                                          float* __restrict__ logits) {
-  __shared__ float xs[kTT][kKC + 1];             // x tile: xs[t][i], padded against conflicts
-  __shared__ __align__(16) float ws[kKC][kTE];   // Wg tile: ws[i][e]
+__global__ void __launch_bounds__(256) gate_logits_scalar_kernel(const Tin* __restrict__ x,
+                                                                 const float* __restrict__ Wg,
+                                                                 int T, int d, int E,
+                                                                 float* __restrict__ logits) {
+  __shared__ float xs[kTT][kKC + 1];
+  __shared__ __align__(16) float ws[kKC][kTE];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
   float acc[4][4];
@@ -36,10 +149,8 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
-
   for (int k0 = 0; k0 < d; k0 += kKC) {
     const int kc = min(kKC, d - k0);
-    // stage x[t0 .. t0+63][k0 .. k0+kc) and Wg[k0 .. k0+kc)[e0 .. e0+63]
     for (int q = threadIdx.x; q < kTT * kKC; q += 256) {
       int tt = q / kKC, kk = q % kKC;
       int t = t0 + tt;
@@ -51,10 +162,9 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
       ws[kk][ee] = (e < E && kk < kc) ? Wg[(size_t)(k0 + kk) * E + e] : 0.0f;
     }
     __syncthreads();
-    for (int kk = 0; kk < kc; ++kk) {            // ascending i, no padding steps
-      float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+    for (int kk = 0; kk < kc; ++kk) {
       float av[4] = {xs[ty * 4][kk], xs[ty * 4 + 1][kk], xs[ty * 4 + 2][kk], xs[ty * 4 + 3][kk]};
-      float bv[4] = {b.x, b.y, b.z, b.w};
+      float bv[4] = {ws[kk][tx * 4], ws[kk][tx * 4 + 1], ws[kk][tx * 4 + 2], ws[kk][tx * 4 + 3]};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -144,12 +254,18 @@ __global__ void __launch_bounds__(256) softmax_topk_kernel(const float* __restri
 cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, int T, int d, int E,
                                float* logits, cudaStream_t s) {
   dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);
-  if (dtype_f16)
-    gate_logits_kernel<__half><<<grid, 256, 0, s>>>(static_cast<const __half*>(x), Wg, T, d, E,
-                                                   logits);
-  else
-    gate_logits_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), Wg, T, d, E,
-                                                  logits);
+  const bool vec = d % 8 == 0 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(Wg) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+  if (dtype_f16) {
+    const __half* xh = static_cast<const __half*>(x);
+    if (vec) gate_logits_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
+    else gate_logits_scalar_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
+  } else {
+    const float* xf = static_cast<const float*>(x);
+    if (vec) gate_logits_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
+    else gate_logits_scalar_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
+  }
   return cudaGetLastError();
 }
 

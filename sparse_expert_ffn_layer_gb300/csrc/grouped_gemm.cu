@@ -34,7 +34,7 @@ constexpr int kBK = 64;           // K per pipeline stage (one 128-byte swizzle 
 constexpr int kABytes = kBM * kBK * 2;
 
 struct SmemLayout {
-  uint32_t stage_bytes, b_off, bars_off, misc_off, total;
+  uint32_t stage_bytes, b_off, bars_off, misc_off, rows_off, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int nmax, int stages, int E) {
@@ -45,7 +45,9 @@ __host__ __device__ inline SmemLayout smem_layout(int nmax, int stages, int E) {
   L.bars_off = off;
   off += (uint32_t)(2 * stages + 4) * 8u;
   L.misc_off = off;
-  off += 16u + 4u * (uint32_t)(E + 1);       // tmem base, abort flag, chunk prefix
+  off += 16u + 8u * (uint32_t)(E + 1);       // tmem base, abort flag, chunk prefix, offsets
+  L.rows_off = off;
+  off += 4u * 2u * 4u * (uint32_t)nmax;      // epilogue: per warp [nmax] tokens and gate weights
   L.total = off + 1024u;                     // slack for 1024-byte alignment
   return L;
 }
@@ -108,6 +110,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.misc_off + 16);
+  int32_t* soffs = prefix + (a.E + 1);                     // copy of offsets[0 .. E]
+  int32_t* row_tok = reinterpret_cast<int32_t*>(smem + L.rows_off);   // [4 warps][nmax]
+  float* row_w = reinterpret_cast<float*>(row_tok + 4 * a.nmax);      // [4 warps][nmax]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -134,11 +139,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(tmem_holder, 2 * a.acc_cols);
   // chunk prefix over experts (warp 2), E <= 1024
   if (warp == 2) {
+    for (int e = lane; e <= a.E; e += 32) soffs[e] = a.offsets[e];
+    __syncwarp();
     const int per = (a.E + 31) / 32;
     const int e_lo = lane * per, e_hi = min(a.E, e_lo + per);
     int local = 0;
     for (int e = e_lo; e < e_hi; ++e) {
-      const int kept = a.offsets[e + 1] - a.offsets[e];
+      const int kept = soffs[e + 1] - soffs[e];
       local += (kept + a.nmax - 1) / a.nmax;
     }
     int incl = local;
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = incl - local;
     for (int e = e_lo; e < e_hi; ++e) {
       prefix[e] = run;
-      const int kept = a.offsets[e + 1] - a.offsets[e];
+      const int kept = soffs[e + 1] - soffs[e];
       run += (kept + a.nmax - 1) / a.nmax;
     }
     if (lane == 31) prefix[a.E] = incl;
@@ -170,27 +177,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0;
+    // this lane's gather rows (first GEMM): groups g = lane, lane + 32 of four rows each;
+    // the next tile's rows are fetched while the current tile streams
+    auto load_rows = [&](const Tile& t, int (&rows)[2][4]) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = 4 * (lane + 32 * h) + q;
+          const int src = t.row0 + (r < t.n ? r : 0);
+          rows[h][q] = t.res ? src : a.perm[src];
+        }
+    };
+    int rows[2][4], rows_next[2][4];
+    if (kGatherB && blockIdx.x < total) load_rows(decode(blockIdx.x / ksplit, a, prefix, soffs), rows);
     for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x) {
-      const Tile t = decode(i / ksplit, a, prefix, a.offsets);
+      const Tile t = decode(i / ksplit, a, prefix, soffs);
       const int ks = i - (i / ksplit) * ksplit;
       const int npad = max(16, (t.n + 15) & ~15);
       const CUtensorMap* mA = t.res ? &tmA_res : &tmA;
       const CUtensorMap* mB = t.res ? &tmB_res : &tmB;
       const int a_y0 = t.res ? 0 : t.e * a.a_rows_per_expert;
       const int a_x = t.mt * kBM;
-      // this lane's gather rows (GEMM1): groups g = lane, lane + 32 of four rows each
-      int rows[2][4];
-      if (kGatherB) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            int r = 4 * (lane + 32 * h) + q;
-            int rr = r < t.n ? r : 0;
-            int src = t.row0 + rr;
-            rows[h][q] = t.res ? src : a.perm[src];
-          }
-      }
+      if (kGatherB && i + (int)gridDim.x < total)
+        load_rows(decode((i + gridDim.x) / ksplit, a, prefix, soffs), rows_next);
       const int nkb = t.K / kBK;
       const int kb0 = ks * nkb / ksplit, kb1 = (ks + 1) * nkb / ksplit;
       for (int kb = kb0; kb < kb1; ++kb) {
@@ -227,6 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           phase ^= 1u;
         }
       }
+      if (kGatherB) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) rows[h][q] = rows_next[h][q];
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -234,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int local = 0;
     for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++local) {
-      const Tile t = decode(i / ksplit, a, prefix, a.offsets);
+      const Tile t = decode(i / ksplit, a, prefix, soffs);
       const int ks = i - (i / ksplit) * ksplit;
       const int npad = max(16, (t.n + 15) & ~15);
       const int buf = local & 1;
@@ -298,10 +314,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int local = 0;
     for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++local) {
-      const Tile t = decode(i / ksplit, a, prefix, a.offsets);
+      const Tile t = decode(i / ksplit, a, prefix, soffs);
       const int ks = i - (i / ksplit) * ksplit;
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1) & 1u;
+      // second GEMM: each warp stages the tile's tokens and gate weights in its own shared
+      // memory while the accumulator is still being computed (a load per row per warp
+      // instead of one per row per thread; warp-private, so no cross-warp barrier)
+      const bool scatter = kEpi == kEpiCombine && !t.res && a.mode != kModeExpertOut && ksplit == 1;
+      int32_t* rt = row_tok + quarter * a.nmax;
+      float* rw = row_w + quarter * a.nmax;
+      if (scatter) {
+        for (int r = lane; r < t.n; r += 32) {
+          rt[r] = a.perm[t.row0 + r];
+          rw[r] = a.slot_w[t.row0 + r];
+        }
+      }
+      __syncwarp();
       bool ok = true;
       if (lane == 0) ok = mbar_wait_bounded(&acc_full[buf], use, abort_flag, a.status, a.wait_ns);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -330,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (a.mode == kModeExpertOut) {
               a.out[(size_t)row * a.ldo + m] = __float2half_rn(v[j]);
             } else {
-              const int tok = a.perm[row];
-              const float w = a.slot_w[row];
+              const int tok = rt[s];
+              const float w = rw[s];
               if (a.mode == kModeDirect) a.out[(size_t)tok * a.ldo + m] = __float2half_rn(w * v[j]);
               else red_add_f32(a.acc32 + (size_t)tok * a.ldo + m, w * v[j]);
             }
