@@ -201,6 +201,29 @@ MOE_API moe_status moe_selftest_wait(void* workspace, uint64_t timeout_ns, moe_s
 #define MOE_STAGE_EVENTS 7
 MOE_API moe_status moe_set_stage_events(void* const* events, int n_events);
 
+/*
+ * Allocation-free variant of moe_expert_ffn (the pages have no counterpart).
+ *
+ * For callers that cannot allocate device memory where they run the layer: a plugin or
+ * custom operator inside a host framework that owns all device memory and gives its
+ * plugins no workspace, or a serving loop that forbids cudaMalloc after start-up because it
+ * can synchronise the device.  They pass inputs and outputs only; the scratch (the hidden
+ * activations H [S_max, f]) lives in a fixed 64 MiB array compiled into the library, which
+ * every GPU that loads the library keeps until the process exits.
+ *   Arguments and results: as moe_expert_ffn, without the workspace.
+ *   Limit: 256 + S_max * f * sizeof(dtype) <= 64 MiB, else MOE_ERR_WORKSPACE (nothing runs).
+ *   The first call on each device looks up the array's device address (with that device
+ *   current); make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents: calls that
+ *   overlap on the GPU race on it (order them on one stream).  Device-side wait timeouts
+ *   are not reported by this variant (it has no status word to read).
+ *   Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+MOE_API moe_status moe_expert_ffn_noalloc(const void* tokens, const int32_t* perm,
+                                          const int32_t* offsets, const void* W1, const void* W2,
+                                          moe_dtype dtype, int T, int d, int f, int E, int S_max,
+                                          void* expert_out, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,8 @@ MOE_MLP_STANDARD, MOE_MLP_RESIDUAL = 0, 1
 
 EXPORTED = ("moe_capacity", "moe_workspace_size", "moe_gate_topk", "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_status_read",
-            "moe_status_string", "moe_selftest_wait", "moe_set_stage_events")
+            "moe_status_string", "moe_selftest_wait", "moe_set_stage_events",
+            "moe_expert_ffn_noalloc")
 
 _lib = None
 MOE_STAGE_EVENTS = 7
@@ -51,6 +52,7 @@ def get_lib():
         "moe_status_string": ([I], ctypes.c_char_p),
         "moe_selftest_wait": ([P, ctypes.c_uint64, P], I),
         "moe_set_stage_events": ([P, I], I),
+        "moe_expert_ffn_noalloc": ([P, P, P, P, P, I, I, I, I, I, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -181,3 +183,13 @@ def moe_set_stage_events(events=None):
         raise ValueError("moe_set_stage_events needs 7 created events (record each once first)")
     arr = (ctypes.c_void_p * MOE_STAGE_EVENTS)(*[ctypes.c_void_p(h) for h in handles])
     _check(get_lib().moe_set_stage_events(arr, MOE_STAGE_EVENTS), "moe_set_stage_events")
+
+
+def moe_expert_ffn_noalloc(tokens, perm, offsets, W1, W2, S_max, expert_out, stream=None):
+    """moe_expert_ffn with the library's fixed scratch instead of a workspace (no allocation)."""
+    T, d = tokens.shape
+    E, _, f = W1.shape
+    _check(get_lib().moe_expert_ffn_noalloc(_ptr(tokens), _ptr(perm), _ptr(offsets), _ptr(W1),
+                                            _ptr(W2), _dtype(tokens), T, d, f, E, S_max,
+                                            _ptr(expert_out), _stream(stream)),
+           "moe_expert_ffn_noalloc")

@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["api.cu", "gate.cu", "dispatch.cu", "grouped_gemm.cu", "simt_ffn.cu", "elementwise.cu"]
+SOURCES = ["api.cu", "gate.cu", "dispatch.cu", "grouped_gemm.cu", "simt_ffn.cu", "elementwise.cu",
+           "noalloc.cu"]
 HEADERS = ["common.cuh", "launch.h", os.path.join("..", "..", "include", "moe.h")]
 
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -306,6 +306,51 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
 
 }  // namespace
 
+namespace moe {
+
+// Argument checks of the allocation-free expert FFN (noalloc.cu): those of moe_expert_ffn
+// without the workspace.
+moe_status expert_ffn_check(const void* tokens, const int32_t* perm, const int32_t* offsets,
+                            const void* W1, const void* W2, moe_dtype dtype, int T, int d, int f,
+                            int E, int S_max, const void* expert_out) {
+  moe_status st = check_shape(T, d, f, E, 1, dtype);
+  if (st != MOE_OK) return st;
+  if (S_max < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0 || S_max == 0) return MOE_OK;
+  if (!tokens || !perm || !offsets || !W1 || !W2 || !expert_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(tokens) || !aligned16(W1) || !aligned16(W2) || !aligned16(expert_out))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// The expert FFN on a given scratch area holding H [S_max, f]; status may be null.
+moe_status expert_ffn_on_scratch(const void* tokens, const int32_t* perm, const int32_t* offsets,
+                                 const void* W1, const void* W2, moe_dtype dtype, int T, int d,
+                                 int f, int E, int S_max, void* expert_out, uint8_t* scratch,
+                                 int* status, cudaStream_t s) {
+  if (dtype == MOE_F16) {
+    return run_tc_ffn(tokens, perm, offsets, W1, W2, nullptr, nullptr, T, d, f, E, 0, S_max, S_max,
+                      reinterpret_cast<__half*>(scratch), nullptr, kModeExpertOut, expert_out,
+                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, s);
+  }
+  SimtArgs a;
+  memset(&a, 0, sizeof(a));
+  a.x = static_cast<const float*>(tokens);
+  a.offsets = offsets;
+  a.perm = perm;
+  a.W1 = static_cast<const float*>(W1);
+  a.W2 = static_cast<const float*>(W2);
+  a.T = T; a.d = d; a.f = f; a.E = E;
+  a.H = reinterpret_cast<float*>(scratch);
+  a.mode = kModeExpertOut;
+  a.out = static_cast<float*>(expert_out);
+  MOE_TRY(launch_simt_ffn1(a, S_max, s));
+  MOE_TRY(launch_simt_ffn2(a, S_max, s));
+  return MOE_OK;
+}
+
+}  // namespace moe
+
 extern "C" {
 
 int moe_capacity(int T, int E, float capacity_factor) { return capacity_of(T, E, capacity_factor); }
