@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
     const int kc = min(kKC, d - k0);
     const bool more = k0 + kKC < d;
     if (more) fetch(k0 + kKC);
-    for (int kk = 0; kk < kc; ++kk) {            // ascending i, no padding steps
+    auto step = [&](int kk) {                      // one i: 16 chained multiply-adds
       const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][tx * 4]);
       const float av[4] = {xs[buf][ty * 4][kk], xs[buf][ty * 4 + 1][kk], xs[buf][ty * 4 + 2][kk],
                            xs[buf][ty * 4 + 3][kk]};
@@ -106,6 +106,12 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+    };
+    if (kc == kKC) {                               // full chunk: straight-line code
+#pragma unroll
+      for (int kk = 0; kk < kKC; ++kk) step(kk);   // ascending i
+    } else {
+      for (int kk = 0; kk < kc; ++kk) step(kk);    // ascending i, no padding steps
     }
     if (more) stash(buf ^ 1);
     __syncthreads();
