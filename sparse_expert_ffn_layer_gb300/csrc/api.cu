@@ -154,18 +154,33 @@ uint32_t pow2_at_least(uint32_t v) {
 
 // Plan of the two tensor-core launches for groups whose tiles hold <= rows_bound rows.
 struct TcPlan {
-  int nmax, stages, grid;
+  int nmax, grid, smem_optin;
   uint32_t acc_cols;
 };
 
-bool tc_plan(int rows_bound, int E, TcPlan* p) {
+bool tc_plan(int rows_bound, TcPlan* p) {
   Dev dv;
   if (!dev_props(&dv)) return false;
   p->nmax = std::min(256, std::max(16, (rows_bound + 15) / 16 * 16));
   p->acc_cols = pow2_at_least((uint32_t)p->nmax);
-  p->stages = gemm_stages_for(p->nmax, E, dv.smem_optin);
   p->grid = dv.sms;
-  return p->stages >= 2;
+  p->smem_optin = dv.smem_optin;
+  return true;
+}
+
+// Weight blocks per item of one GEMM (1, 2 or 4 adjacent 128-row blocks sharing one gather of
+// the token rows): the widest that divides every group's M, fits TMEM (two buffers) and
+// three pipeline stages, and still leaves about six waves of items.
+int choose_mw(long long row_tiles, int M_exp, long long res_tiles, int M_res, const TcPlan& p,
+              int E) {
+  for (int mw = 4; mw >= 2; mw /= 2) {
+    if (M_exp % (128 * mw) || (res_tiles && M_res % (128 * mw))) continue;
+    if (2u * (uint32_t)mw * p.acc_cols > 512u) continue;
+    if (gemm_stages_for(p.nmax, E, mw, p.smem_optin) < 3) continue;
+    const long long items = row_tiles * (M_exp / (128 * mw)) + res_tiles * (M_res / (128 * mw));
+    if (items >= 6LL * p.grid) return mw;
+  }
+  return 1;
 }
 
 // Chunks per tile so that a launch has about four waves of work items, each chunk keeping at
@@ -180,11 +195,12 @@ int choose_ksplit(long long items_bound, int nkb_min, int sms) {
 // TMA boxes of 64 K-rows produce: M-blocks 8 KB apart, 8-row K groups 1 KB apart.
 constexpr uint32_t kALbo = 8192, kASbo = 1024;
 
-void fill_common(GemmArgs& g, const TcPlan& p, int E, int* status) {
+void fill_common(GemmArgs& g, const TcPlan& p, int E, int mw, int* status) {
   memset(&g, 0, sizeof(g));
   g.E = E;
   g.nmax = p.nmax;
-  g.stages = p.stages;
+  g.mw = mw;
+  g.stages = gemm_stages_for(p.nmax, E, mw, p.smem_optin);
   g.acc_cols = p.acc_cols;
   g.a_lbo = kALbo;
   g.a_sbo = kASbo;
@@ -215,16 +231,18 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
                       size_t partial_bytes, int* status, cudaStream_t s) {
   const bool residual = Wr1 != nullptr;
   TcPlan plan;
-  if (!tc_plan(rows_bound, E, &plan)) return MOE_ERR_CUDA;
+  if (!tc_plan(rows_bound, &plan)) return MOE_ERR_CUDA;
   const int T_res = residual ? T : 0;
   const int part_rows = S_rows + T_res;
   const long long tiles_bound = std::min(E, S_rows) + S_rows / plan.nmax;
   const long long res_tiles = residual ? (T + plan.nmax - 1) / plan.nmax : 0;
+  const int mw1 = choose_mw(tiles_bound, f, res_tiles, f_res, plan, E);
+  const int mw2 = choose_mw(tiles_bound, d, res_tiles, d, plan, E);
   int ks1 = 1, ks2 = 1;
   if (partial) {
-    ks1 = choose_ksplit(tiles_bound * (f / 128) + res_tiles * (residual ? f_res / 128 : 0), d / 64,
-                        plan.grid);
-    ks2 = choose_ksplit((tiles_bound + res_tiles) * (d / 128),
+    ks1 = choose_ksplit(tiles_bound * (f / 128 / mw1) + res_tiles * (residual ? f_res / 128 / mw1 : 0),
+                        d / 64, plan.grid);
+    ks2 = choose_ksplit((tiles_bound + res_tiles) * (d / 128 / mw2),
                         residual ? std::min(f, f_res) / 64 : f / 64, plan.grid);
     const size_t cols1 = std::max(f, residual ? f_res : 0);
     if ((size_t)ks1 * part_rows * cols1 * 4 > partial_bytes) ks1 = 1;
@@ -245,14 +263,15 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
     mHres = mH;
   }
   GemmArgs g1;
-  fill_common(g1, plan, E, status);
+  fill_common(g1, plan, E, mw1, status);
+  if (g1.stages < 2) return MOE_ERR_UNSUPPORTED;
   g1.offsets = offsets;
   g1.perm = perm;
   g1.n_res_rows = residual ? T : 0;
   g1.K = d;
   g1.K_res = d;
-  g1.mt_exp = f / 128;
-  g1.mt_res = residual ? f_res / 128 : 1;
+  g1.mt_exp = f / 128 / mw1;
+  g1.mt_res = residual ? f_res / 128 / mw1 : 1;
   g1.a_rows_per_expert = d;
   g1.h_out = H;
   g1.ldh = f;
@@ -278,14 +297,15 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   MOE_TRY(stage_mark(4, s));
 
   GemmArgs g2;
-  fill_common(g2, plan, E, status);
+  fill_common(g2, plan, E, mw2, status);
+  if (g2.stages < 2) return MOE_ERR_UNSUPPORTED;
   g2.offsets = offsets;
   g2.perm = perm;
   g2.n_res_rows = residual ? T : 0;
   g2.K = f;
   g2.K_res = f_res;
-  g2.mt_exp = d / 128;
-  g2.mt_res = d / 128;
+  g2.mt_exp = d / 128 / mw2;
+  g2.mt_res = d / 128 / mw2;
   g2.a_rows_per_expert = f;
   g2.mode = mode;
   g2.out = static_cast<__half*>(out);

@@ -29,18 +29,18 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kBM = 128;          // MMA M (weight rows per tile)
+constexpr int kBM = 128;          // MMA M (weight rows per accumulator)
 constexpr int kBK = 64;           // K per pipeline stage (one 128-byte swizzle span of f16)
-constexpr int kABytes = kBM * kBK * 2;
+constexpr int kABytes = kBM * kBK * 2;   // one 128-row A block per stage; an item has mw of them
 
 struct SmemLayout {
   uint32_t stage_bytes, b_off, bars_off, misc_off, rows_off, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int nmax, int stages, int E) {
+__host__ __device__ inline SmemLayout smem_layout(int nmax, int stages, int E, int mw) {
   SmemLayout L;
-  L.b_off = kABytes;
-  L.stage_bytes = kABytes + (uint32_t)nmax * 128u;
+  L.b_off = (uint32_t)mw * kABytes;
+  L.stage_bytes = L.b_off + (uint32_t)nmax * 128u;
   uint32_t off = (uint32_t)stages * L.stage_bytes;
   L.bars_off = off;
   off += (uint32_t)(2 * stages + 4) * 8u;
@@ -102,7 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = smem_layout(a.nmax, a.stages, a.E);
+  const SmemLayout L = smem_layout(a.nmax, a.stages, a.E, a.mw);
+  const int mw = a.mw;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off);
   uint64_t* empty = full + a.stages;
   uint64_t* acc_full = empty + a.stages;     // [2]
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmB_res);
     }
   }
-  if (warp == 1) tmem_alloc(tmem_holder, 2 * a.acc_cols);
+  if (warp == 1) tmem_alloc(tmem_holder, 2 * mw * a.acc_cols);
   // chunk prefix over experts (warp 2), E <= 1024
   if (warp == 2) {
     for (int e = lane; e <= a.E; e += 32) soffs[e] = a.offsets[e];
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* mA = t.res ? &tmA_res : &tmA;
       const CUtensorMap* mB = t.res ? &tmB_res : &tmB;
       const int a_y0 = t.res ? 0 : t.e * a.a_rows_per_expert;
-      const int a_x = t.mt * kBM;
+      const int a_x = t.mt * mw * kBM;
       if (kGatherB && i + (int)gridDim.x < total)
         load_rows(decode((i + gridDim.x) / ksplit, a, prefix, soffs), rows_next);
       const int nkb = t.K / kBK;
@@ -211,12 +212,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* sA = smem + (size_t)stage * L.stage_bytes;
         uint8_t* sB = sA + L.b_off;
         if (lane == 0) {
-          mbar_expect_tx(&full[stage], (uint32_t)kABytes + (uint32_t)npad * 128u);
+          mbar_expect_tx(&full[stage], (uint32_t)(mw * kABytes) + (uint32_t)npad * 128u);
         }
         __syncwarp();
         if (lane == 0) {
-          tma_load_2d(sA, mA, a_x, a_y0 + kb * kBK, &full[stage]);
-          tma_load_2d(sA + kABytes / 2, mA, a_x + 64, a_y0 + kb * kBK, &full[stage]);
+          for (int h = 0; h < mw; ++h) {               // mw adjacent 128-row blocks
+            tma_load_2d(sA + h * kABytes, mA, a_x + h * kBM, a_y0 + kb * kBK, &full[stage]);
+            tma_load_2d(sA + h * kABytes + kABytes / 2, mA, a_x + h * kBM + 64, a_y0 + kb * kBK,
+                        &full[stage]);
+          }
         }
         if (kGatherB) {
 #pragma unroll
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)buf * a.acc_cols;
+      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * mw) * a.acc_cols;
       const uint32_t idesc = idesc_f16(kBM, npad, 1, 0);
       const int nkb = t.K / kBK;
       const int kb0 = ks * nkb / ksplit, kb1 = (ks + 1) * nkb / ksplit;
@@ -274,9 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = a0 + L.b_off;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = smem_desc(a0 + kk * 2048, a.a_lbo, a.a_sbo, 2);
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
-            tc_mma_f16(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+            for (int h = 0; h < mw; ++h) {             // same token rows, mw weight blocks
+              const uint64_t ad = smem_desc(a0 + h * kABytes + kk * 2048, a.a_lbo, a.a_sbo, 2);
+              tc_mma_f16(d_tmem + (uint32_t)h * a.acc_cols, ad, bd, idesc,
+                         (kb != kb0 || kk != 0) ? 1u : 0u);
+            }
           }
           tc_commit(&empty[stage]);        // frees the stage once these MMAs have read it
         }
@@ -336,8 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const int m = t.mt * kBM + row_in_tile;
-      const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)buf * a.acc_cols;
+      for (int h = 0; h < mw; ++h) {
+      const int m = (t.mt * mw + h) * kBM + row_in_tile;
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) +
+                             (uint32_t)(buf * mw + h) * a.acc_cols;
       for (int c0 = 0; c0 < t.n; c0 += 16) {
         float v[16];
         tmem_ld16(taddr + (uint32_t)c0, v);
@@ -367,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
     }
@@ -388,13 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, 2 * a.acc_cols);
+  if (warp == 1) tmem_dealloc(tmem_base, 2 * mw * a.acc_cols);
 }
 
 template <bool G, int Epi>
 cudaError_t launch_one(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                        const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s) {
-  const SmemLayout L = smem_layout(args.nmax, args.stages, args.E);
+  const SmemLayout L = smem_layout(args.nmax, args.stages, args.E, args.mw);
   cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<G, Epi>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
   if (err != cudaSuccess) return err;
@@ -404,9 +414,9 @@ cudaError_t launch_one(const CUtensorMap& A, const CUtensorMap& B, const CUtenso
 
 }  // namespace
 
-int gemm_stages_for(int nmax, int E, int smem_limit) {
+int gemm_stages_for(int nmax, int E, int mw, int smem_limit) {
   for (int st = 8; st >= 2; --st)
-    if ((int)smem_layout(nmax, st, E).total <= smem_limit) return st;
+    if ((int)smem_layout(nmax, st, E, mw).total <= smem_limit) return st;
   return 0;
 }
 

@@ -21,7 +21,9 @@ struct GemmArgs {
   int E;
   int n_res_rows;           // rows of the residual group (T), 0 when absent
   int K, K_res;             // shared dimension of expert / residual tiles
-  int mt_exp, mt_res;       // M-tiles (of 128) per expert / residual tile
+  int mt_exp, mt_res;       // M items (of mw x 128 rows) per expert / residual row tile
+  int mw;                   // 128-row weight blocks per item (1, 2 or 4): one TMEM
+                            // accumulator each, all fed by the same gathered token rows
   int a_rows_per_expert;    // rows of the A tensor map per expert
   int nmax;                 // rows per tile, multiple of 16, <= 256
   int stages;               // pipeline depth
@@ -68,7 +70,7 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C,
                             int32_t* counts_raw, int32_t* kept, int32_t* offsets, int32_t* perm,
                             int32_t* slot_of, const float* topk_w, float* slot_w, cudaStream_t s);
 
-int gemm_stages_for(int nmax, int E, int smem_limit);
+int gemm_stages_for(int nmax, int E, int mw, int smem_limit);
 cudaError_t launch_grouped_gemm1(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                                  const CUtensorMap& Br, const GemmArgs& args, int grid,
                                  cudaStream_t s);
