@@ -22,7 +22,12 @@ namespace {
 
 constexpr int kWarps = 32;
 constexpr int kUnroll = 8;      // batches of 32 assignments whose loads are issued together
+constexpr int kRegBatches = 8;  // runs of up to 8 x 32 assignments per warp stay in registers
 
+// kReg > 0: each warp's run (<= 32 kReg assignments) is loaded once and its experts, local
+// ranks and gate weights stay in registers from pass 1 to pass 3.  kReg == 0: any length;
+// local ranks go through slot_of.
+template <int kReg>
 __global__ void __launch_bounds__(1024) dispatch_kernel(
     const int32_t* __restrict__ topk_idx, int n, int k, int E, int C,
     int32_t* __restrict__ counts_raw, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
@@ -40,20 +45,22 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
   const int a_begin = min(n, w * L), a_end = min(n, a_begin + L);
   const unsigned lt_mask = (1u << lane) - 1u;
 
-  // pass 1: rank inside the warp's run; kept temporarily in slot_of.  Eight batches of 32
-  // assignments are fetched at once so their loads overlap.
-  for (int base = a_begin; base < a_end; base += 32 * kUnroll) {
-    int ev[kUnroll];
+  // pass 1: rank inside the warp's run
+  int ev_r[kReg > 0 ? kReg : 1], rv_r[kReg > 0 ? kReg : 1];
+  float wv_r[kReg > 0 ? kReg : 1];
+  if (kReg > 0) {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int a = base + 32 * u + lane;
-      ev[u] = a < a_end ? topk_idx[a] : -1;
+    for (int u = 0; u < kReg; ++u) {                     // one burst of loads for the whole run
+      const int a = a_begin + 32 * u + lane;
+      ev_r[u] = a < a_end ? topk_idx[a] : -1;
+      wv_r[u] = (a < a_end && slot_w) ? topk_w[a] : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (base + 32 * u >= a_end) break;                 // warp-uniform
-      const int a = base + 32 * u + lane;
-      int e = ev[u];
+    for (int u = 0; u < kReg; ++u) {
+      rv_r[u] = 0;
+      if (a_begin + 32 * u >= a_end) continue;           // warp-uniform
+      const int a = a_begin + 32 * u + lane;
+      int e = ev_r[u];
       const bool valid = a < a_end && (unsigned)e < (unsigned)E;   // out-of-range: dropped
       if (!valid) e = -1 - lane;                         // invalid lanes form singleton groups
       const unsigned grp = __match_any_sync(0xffffffffu, e);
@@ -62,10 +69,38 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
       if (valid) before = cnt[w * E + e];
       __syncwarp();
       if (valid) {
-        slot_of[a] = before + __popc(grp & lt_mask);
+        rv_r[u] = before + __popc(grp & lt_mask);
         if (lane == leader) cnt[w * E + e] = before + __popc(grp);
       }
       __syncwarp();
+    }
+  } else {
+    // local ranks are kept temporarily in slot_of; eight batches of loads in flight
+    for (int base = a_begin; base < a_end; base += 32 * kUnroll) {
+      int ev[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int a = base + 32 * u + lane;
+        ev[u] = a < a_end ? topk_idx[a] : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (base + 32 * u >= a_end) break;               // warp-uniform
+        const int a = base + 32 * u + lane;
+        int e = ev[u];
+        const bool valid = a < a_end && (unsigned)e < (unsigned)E;
+        if (!valid) e = -1 - lane;
+        const unsigned grp = __match_any_sync(0xffffffffu, e);
+        const int leader = __ffs(grp) - 1;
+        int before = 0;
+        if (valid) before = cnt[w * E + e];
+        __syncwarp();
+        if (valid) {
+          slot_of[a] = before + __popc(grp & lt_mask);
+          if (lane == leader) cnt[w * E + e] = before + __popc(grp);
+        }
+        __syncwarp();
+      }
     }
   }
   __syncthreads();
@@ -115,32 +150,43 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
   }
   __syncthreads();
 
-  // pass 3: global rank -> slot (again eight batches of loads in flight)
-  for (int base = a_begin; base < a_end; base += 32 * kUnroll) {
-    int ev[kUnroll], rv[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int a = base + 32 * u + lane;
-      ev[u] = a < a_end ? topk_idx[a] : -1;
-      rv[u] = a < a_end ? slot_of[a] : 0;
+  // pass 3: global rank -> slot
+  auto place = [&](int a, int e, int rank_local, float wgt) {
+    if ((unsigned)e >= (unsigned)E) {
+      slot_of[a] = -1;
+      return;
     }
+    const int r = cnt[w * E + e] + rank_local;
+    if (r < C) {
+      const int s = offs[e] + r;
+      slot_of[a] = s;
+      perm[s] = a / k;
+      if (slot_w) slot_w[s] = wgt;
+    } else {
+      slot_of[a] = -1;
+    }
+  };
+  if (kReg > 0) {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int a = base + 32 * u + lane;
-      if (a >= a_end) continue;
-      const int e = ev[u];
-      if ((unsigned)e >= (unsigned)E) {
-        slot_of[a] = -1;
-        continue;
+    for (int u = 0; u < kReg; ++u) {
+      const int a = a_begin + 32 * u + lane;
+      if (a < a_end) place(a, ev_r[u], rv_r[u], wv_r[u]);
+    }
+  } else {
+    for (int base = a_begin; base < a_end; base += 32 * kUnroll) {
+      int ev[kUnroll], rv[kUnroll];
+      float wv[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int a = base + 32 * u + lane;
+        ev[u] = a < a_end ? topk_idx[a] : -1;
+        rv[u] = a < a_end ? slot_of[a] : 0;
+        wv[u] = (a < a_end && slot_w) ? topk_w[a] : 0.f;
       }
-      const int r = cnt[w * E + e] + rv[u];
-      if (r < C) {
-        const int s = offs[e] + r;
-        slot_of[a] = s;
-        perm[s] = a / k;
-        if (slot_w) slot_w[s] = topk_w[a];
-      } else {
-        slot_of[a] = -1;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int a = base + 32 * u + lane;
+        if (a < a_end) place(a, ev[u], rv[u], wv[u]);
       }
     }
   }
@@ -153,11 +199,13 @@ size_t dispatch_smem_bytes(int E) { return sizeof(int32_t) * ((size_t)kWarps * E
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C, int32_t* counts_raw,
                             int32_t* kept, int32_t* offsets, int32_t* perm, int32_t* slot_of,
                             const float* topk_w, float* slot_w, cudaStream_t s) {
-  size_t smem = dispatch_smem_bytes(E);
-  cudaError_t err = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+  const size_t smem = dispatch_smem_bytes(E);
+  const int n = T * k;
+  const bool in_regs = (n + kWarps - 1) / kWarps <= 32 * kRegBatches;
+  auto kern = in_regs ? dispatch_kernel<kRegBatches> : dispatch_kernel<0>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  dispatch_kernel<<<1, kWarps * 32, smem, s>>>(topk_idx, T * k, k, E, C, counts_raw, kept, offsets,
+  kern<<<1, kWarps * 32, smem, s>>>(topk_idx, n, k, E, C, counts_raw, kept, offsets,
                                                perm, slot_of, topk_w, slot_w);
   return cudaGetLastError();
 }

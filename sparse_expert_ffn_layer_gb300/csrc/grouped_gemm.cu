@@ -94,7 +94,7 @@ __device__ __forceinline__ Tile decode(int i, const GemmArgs& a, const int32_t* 
   return t;
 }
 
-template <bool kGatherB, int kEpi>
+template <bool kGatherB, int kEpi, int kMW>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmA_res,
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const SmemLayout L = smem_layout(a.nmax, a.stages, a.E, a.mw);
-  const int mw = a.mw;
+  constexpr int mw = kMW;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off);
   uint64_t* empty = full + a.stages;
   uint64_t* acc_full = empty + a.stages;     // [2]
@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) {
+#pragma unroll
           for (int h = 0; h < mw; ++h) {               // mw adjacent 128-row blocks
             tma_load_2d(sA + h * kABytes, mA, a_x + h * kBM, a_y0 + kb * kBK, &full[stage]);
             tma_load_2d(sA + h * kABytes + kABytes / 2, mA, a_x + h * kBM + 64, a_y0 + kb * kBK,
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
+#pragma unroll
             for (int h = 0; h < mw; ++h) {             // same token rows, mw weight blocks
               const uint64_t ad = smem_desc(a0 + h * kABytes + kk * 2048, a.a_lbo, a.a_sbo, 2);
               tc_mma_f16(d_tmem + (uint32_t)h * a.acc_cols, ad, bd, idesc,
@@ -343,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
+#pragma unroll 1
       for (int h = 0; h < mw; ++h) {
       const int m = (t.mt * mw + h) * kBM + row_in_tile;
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) +
@@ -401,15 +404,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, 2 * mw * a.acc_cols);
 }
 
+template <bool G, int Epi, int MW>
+cudaError_t launch_mw(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
+                      const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s) {
+  const SmemLayout L = smem_layout(args.nmax, args.stages, args.E, MW);
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<G, Epi, MW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+  if (err != cudaSuccess) return err;
+  grouped_gemm_kernel<G, Epi, MW><<<grid, kThreads, L.total, s>>>(A, B, Ar, Br, args);
+  return cudaGetLastError();
+}
+
 template <bool G, int Epi>
 cudaError_t launch_one(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                        const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s) {
-  const SmemLayout L = smem_layout(args.nmax, args.stages, args.E, args.mw);
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<G, Epi>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
-  if (err != cudaSuccess) return err;
-  grouped_gemm_kernel<G, Epi><<<grid, kThreads, L.total, s>>>(A, B, Ar, Br, args);
-  return cudaGetLastError();
+  switch (args.mw) {
+    case 1: return launch_mw<G, Epi, 1>(A, B, Ar, Br, args, grid, s);
+    case 2: return launch_mw<G, Epi, 2>(A, B, Ar, Br, args, grid, s);
+    case 4: return launch_mw<G, Epi, 4>(A, B, Ar, Br, args, grid, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
