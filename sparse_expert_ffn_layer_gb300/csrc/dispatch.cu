@@ -9,12 +9,15 @@
 //
 // One block of 32 warps, no atomics.  Warp w owns a contiguous run of the assignment list.
 // Pass 1: each warp walks its run 32 assignments at a time; lanes with equal experts are
-// grouped with __match_any_sync, so the rank inside the warp's run is the warp's running
+// grouped by ballots over the bits of the expert index, so the rank inside the warp's run is the warp's running
 // count for that expert (in shared memory, private to the warp) plus the number of
 // lower lanes in the group.  Pass 2: per expert, an exclusive scan of the 32 warp counts
 // gives each warp's base; kept = min(count, C); a block scan of kept gives the offsets.
 // Pass 3: each assignment's global rank is base + local rank, which decides kept / dropped
-// and the slot.
+// and the slot; perm and the slot weights are assembled in shared memory and written out
+// coalesced.
+#include <algorithm>
+
 #include "launch.h"
 
 namespace moe {
@@ -24,6 +27,18 @@ constexpr int kWarps = 32;
 constexpr int kUnroll = 8;      // batches of 32 assignments whose loads are issued together
 constexpr int kRegBatches = 8;  // runs of up to 8 x 32 assignments per warp stay in registers
 
+// Lanes holding the same expert as this lane (valid lanes only; an invalid lane is alone):
+// one ballot per bit of the expert index, which keeps lanes whose bit agrees.
+__device__ __forceinline__ unsigned match_lanes(int e, bool valid, int nbits, int lane) {
+  unsigned m = __ballot_sync(0xffffffffu, valid);
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned set = __ballot_sync(0xffffffffu, bit && valid);
+    m &= bit ? set : ~set;
+  }
+  return valid ? m : (1u << lane);
+}
+
 // kReg > 0: each warp's run (<= 32 kReg assignments) is loaded once and its experts, local
 // ranks and gate weights stay in registers from pass 1 to pass 3.  kReg == 0: any length;
 // local ranks go through slot_of.
@@ -32,11 +47,14 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
     const int32_t* __restrict__ topk_idx, int n, int k, int E, int C,
     int32_t* __restrict__ counts_raw, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm, int32_t* __restrict__ slot_of, const float* __restrict__ topk_w,
-    float* __restrict__ slot_w) {
+    float* __restrict__ slot_w, int S_cap, int stage_out) {
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;                       // [kWarps][E]: running count, then warp base
   int32_t* offs = sm + kWarps * E;         // [E + 1]
   int32_t* wsum = offs + E + 1;            // [kWarps] scan scratch
+  int32_t* perm_s = wsum + kWarps;         // [S_cap] when stage_out: perm, written out coalesced
+  float* slotw_s = reinterpret_cast<float*>(perm_s + S_cap);   // [S_cap] gate weight per slot
+  const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int q = threadIdx.x; q < kWarps * E; q += blockDim.x) cnt[q] = 0;
   __syncthreads();
@@ -60,10 +78,9 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
       rv_r[u] = 0;
       if (a_begin + 32 * u >= a_end) continue;           // warp-uniform
       const int a = a_begin + 32 * u + lane;
-      int e = ev_r[u];
+      const int e = ev_r[u];
       const bool valid = a < a_end && (unsigned)e < (unsigned)E;   // out-of-range: dropped
-      if (!valid) e = -1 - lane;                         // invalid lanes form singleton groups
-      const unsigned grp = __match_any_sync(0xffffffffu, e);
+      const unsigned grp = match_lanes(e, valid, nbits, lane);
       const int leader = __ffs(grp) - 1;
       int before = 0;
       if (valid) before = cnt[w * E + e];
@@ -87,10 +104,9 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
       for (int u = 0; u < kUnroll; ++u) {
         if (base + 32 * u >= a_end) break;               // warp-uniform
         const int a = base + 32 * u + lane;
-        int e = ev[u];
+        const int e = ev[u];
         const bool valid = a < a_end && (unsigned)e < (unsigned)E;
-        if (!valid) e = -1 - lane;
-        const unsigned grp = __match_any_sync(0xffffffffu, e);
+        const unsigned grp = match_lanes(e, valid, nbits, lane);
         const int leader = __ffs(grp) - 1;
         int before = 0;
         if (valid) before = cnt[w * E + e];
@@ -160,8 +176,13 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
     if (r < C) {
       const int s = offs[e] + r;
       slot_of[a] = s;
-      perm[s] = a / k;
-      if (slot_w) slot_w[s] = wgt;
+      if (stage_out) {
+        perm_s[s] = a / k;
+        if (slot_w) slotw_s[s] = wgt;
+      } else {
+        perm[s] = a / k;
+        if (slot_w) slot_w[s] = wgt;
+      }
     } else {
       slot_of[a] = -1;
     }
@@ -190,23 +211,37 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
       }
     }
   }
+  if (stage_out) {                                       // coalesced copy-out of the slots
+    __syncthreads();
+    const int S = offs[E];
+    for (int q = threadIdx.x; q < S; q += blockDim.x) perm[q] = perm_s[q];
+    if (slot_w)
+      for (int q = threadIdx.x; q < S; q += blockDim.x) slot_w[q] = slotw_s[q];
+  }
 }
 
 }  // namespace
 
 size_t dispatch_smem_bytes(int E) { return sizeof(int32_t) * ((size_t)kWarps * E + E + 1 + kWarps); }
 
+// Slots staged in shared memory when they fit beside the counters.
+constexpr size_t kDispatchSmemMax = 200 * 1024;
+
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C, int32_t* counts_raw,
                             int32_t* kept, int32_t* offsets, int32_t* perm, int32_t* slot_of,
                             const float* topk_w, float* slot_w, cudaStream_t s) {
-  const size_t smem = dispatch_smem_bytes(E);
   const int n = T * k;
+  const int S_cap = (int)std::min<long long>(n, (long long)E * C);
+  size_t smem = dispatch_smem_bytes(E);
+  const size_t staged = smem + (size_t)S_cap * 8;
+  const int stage_out = staged <= kDispatchSmemMax ? 1 : 0;
+  if (stage_out) smem = staged;
   const bool in_regs = (n + kWarps - 1) / kWarps <= 32 * kRegBatches;
   auto kern = in_regs ? dispatch_kernel<kRegBatches> : dispatch_kernel<0>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   kern<<<1, kWarps * 32, smem, s>>>(topk_idx, n, k, E, C, counts_raw, kept, offsets,
-                                               perm, slot_of, topk_w, slot_w);
+                                    perm, slot_of, topk_w, slot_w, S_cap, stage_out);
   return cudaGetLastError();
 }
 

@@ -13,119 +13,103 @@ namespace {
 constexpr int kTT = 64;   // tokens per block tile
 constexpr int kTE = 64;   // experts per block tile
 constexpr int kKC = 32;   // shared-dimension chunk staged in shared memory
+constexpr int kXP = kKC + 4;  // padded row of the token tile (16-byte aligned rows)
 
-// One thread's share of a token chunk: 32 consecutive values of a row.
 template <typename Tin>
-struct XChunk;
+struct XChunk;  // one thread's share of a 64 x 32 token chunk: 8 consecutive values of a row
 
 template <>
 struct XChunk<__half> {
-  uint4 raw[4];
-  __device__ __forceinline__ void load(const __half* p) {
+  uint4 raw;
+  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void zero() { raw = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
+    const __half2* h = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) raw[q] = *reinterpret_cast<const uint4*>(p + 8 * q);
-  }
-  __device__ __forceinline__ void zero() {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) raw[q] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  __device__ __forceinline__ float get(int j) const {   // exact widening
-    const __half2* h = reinterpret_cast<const __half2*>(raw);
-    const float2 f = __half22float2(h[j >> 1]);
-    return (j & 1) ? f.y : f.x;
+    for (int q = 0; q < 4; ++q) {
+      float2 f = __half22float2(h[q]);      // exact widening
+      v[2 * q] = f.x;
+      v[2 * q + 1] = f.y;
+    }
   }
 };
 
 template <>
 struct XChunk<float> {
-  float4 r[8];
+  float4 a, b;
   __device__ __forceinline__ void load(const float* p) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) r[q] = *reinterpret_cast<const float4*>(p + 4 * q);
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 4);
   }
-  __device__ __forceinline__ void zero() {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) r[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  __device__ __forceinline__ float get(int j) const {
-    const float4 v = r[j >> 2];
-    return (j & 3) == 0 ? v.x : (j & 3) == 1 ? v.y : (j & 3) == 2 ? v.z : v.w;
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
   }
 };
 
-constexpr int kGKC = 64;       // shared-dimension chunk of the vector kernel
-constexpr int kXT = kTT + 4;   // padded row of the transposed token tile (16-byte aligned)
-
-size_t gate_smem_bytes() { return sizeof(float) * 2 * kGKC * (kXT + kTE); }
-
-// logits[T, E] = x[T, d] . Wg[d, E]; 128 threads, 8 tokens x 4 experts per thread (32
-// independent chains, each walking i in order).  Token tile stored i-major so each step
-// reads a thread's 8 tokens with two 16-byte loads; the next 64-wide chunk is fetched into
-// registers while the current one is multiplied (about a microsecond of work per chunk,
-// enough to cover an L2 or DRAM round trip).  Needs d % 32 == 0 and E % 4 == 0.
+// logits[T, E] = x[T, d] . Wg[d, E]; 256 threads, 4 x 4 outputs per thread.  The next chunk
+// is fetched into registers while the current one is multiplied (double-buffered tiles).
+// Vector path: d % 8 == 0 and E % 4 == 0 (16-byte loads); otherwise the scalar kernel below.
 template <typename Tin>
-__global__ void __launch_bounds__(128) gate_logits_kernel(const Tin* __restrict__ x,
+__global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict__ x,
                                                           const float* __restrict__ Wg, int T,
                                                           int d, int E,
                                                           float* __restrict__ logits) {
-  extern __shared__ __align__(16) float gsm[];
-  float (*xs)[kGKC][kXT] = reinterpret_cast<float (*)[kGKC][kXT]>(gsm);                 // [2]
-  float (*ws)[kGKC][kTE] = reinterpret_cast<float (*)[kGKC][kTE]>(gsm + 2 * kGKC * kXT);  // [2]
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // experts 4tx.., tokens 8ty..
+  __shared__ __align__(16) float xs[2][kTT][kXP];   // token tile: xs[t][i]
+  __shared__ __align__(16) float ws[2][kKC][kTE];   // Wg tile: ws[i][e]
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
-  // loader roles: token row lt, columns lk .. lk+31; Wg rows lw + 8 r (4 experts at le)
-  const int lt = threadIdx.x >> 1, lk = (threadIdx.x & 1) * 32;
+  // loader roles: token row lt, columns lk .. lk+7; Wg rows lw, lw+16 (4 experts at le)
+  const int lt = threadIdx.x >> 2, lk = (threadIdx.x & 3) * 8;
   const int lw = threadIdx.x >> 4, le = (threadIdx.x & 15) * 4;
-  float acc[8][4];
+  float acc[4][4];
 #pragma unroll
-  for (int a = 0; a < 8; ++a)
+  for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
 
   XChunk<Tin> xr;
-  float4 wr[8];
+  float4 wr0, wr1;
   auto fetch = [&](int k0) {
     const int t = t0 + lt;
-    const int kc = min(kGKC, d - k0);
+    const int kc = min(kKC, d - k0);
     if (t < T && lk < kc) xr.load(x + (size_t)t * d + k0 + lk);
     else xr.zero();
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     const bool eok = e0 + le < E;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int row = lw + 8 * r;
-      wr[r] = (eok && row < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + row) * E + e0 + le)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    wr0 = (eok && lw < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw) * E + e0 + le) : z;
+    wr1 = (eok && lw + 16 < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw + 16) * E + e0 + le) : z;
   };
   auto stash = [&](int buf) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) xs[buf][lk + j][lt] = xr.get(j);
-#pragma unroll
-    for (int r = 0; r < 8; ++r) *reinterpret_cast<float4*>(&ws[buf][lw + 8 * r][le]) = wr[r];
+    float v[8];
+    xr.to_f32(v);
+    *reinterpret_cast<float4*>(&xs[buf][lt][lk]) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(&xs[buf][lt][lk + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+    *reinterpret_cast<float4*>(&ws[buf][lw][le]) = wr0;
+    *reinterpret_cast<float4*>(&ws[buf][lw + 16][le]) = wr1;
   };
 
   fetch(0);
   stash(0);
   __syncthreads();
   int buf = 0;
-  for (int k0 = 0; k0 < d; k0 += kGKC) {
-    const int kc = min(kGKC, d - k0);
-    const bool more = k0 + kGKC < d;
-    if (more) fetch(k0 + kGKC);
-    auto step = [&](int kk) {                      // one i: 32 chained multiply-adds
-      const float4 xa = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * 8]);
-      const float4 xb = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * 8 + 4]);
+  for (int k0 = 0; k0 < d; k0 += kKC) {
+    const int kc = min(kKC, d - k0);
+    const bool more = k0 + kKC < d;
+    if (more) fetch(k0 + kKC);
+    auto step = [&](int kk) {                      // one i: 16 chained multiply-adds
       const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][tx * 4]);
-      const float av[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      const float av[4] = {xs[buf][ty * 4][kk], xs[buf][ty * 4 + 1][kk], xs[buf][ty * 4 + 2][kk],
+                           xs[buf][ty * 4 + 3][kk]};
       const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
     };
-    if (kc == kGKC) {                              // full chunk: straight-line code
+    if (kc == kKC) {                               // full chunk: straight-line code
 #pragma unroll
-      for (int kk = 0; kk < kGKC; ++kk) step(kk);  // ascending i
+      for (int kk = 0; kk < kKC; ++kk) step(kk);   // ascending i
     } else {
       for (int kk = 0; kk < kc; ++kk) step(kk);    // ascending i, no padding steps
     }
@@ -134,8 +118,8 @@ __global__ void __launch_bounds__(128) gate_logits_kernel(const Tin* __restrict_
     buf ^= 1;
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int t = t0 + ty * 8 + i;
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
     if (t >= T) continue;
     const int e = e0 + tx * 4;
     if (e + 3 < E) {
@@ -276,30 +260,17 @@ __global__ void __launch_bounds__(256) softmax_topk_kernel(const float* __restri
 cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, int T, int d, int E,
                                float* logits, cudaStream_t s) {
   dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);
-  const bool vec = d % 32 == 0 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+  const bool vec = d % 8 == 0 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(Wg) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
-  const size_t smem = gate_smem_bytes();
   if (dtype_f16) {
     const __half* xh = static_cast<const __half*>(x);
-    if (vec) {
-      cudaError_t err = cudaFuncSetAttribute(gate_logits_kernel<__half>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (err != cudaSuccess) return err;
-      gate_logits_kernel<__half><<<grid, 128, smem, s>>>(xh, Wg, T, d, E, logits);
-    } else {
-      gate_logits_scalar_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
-    }
+    if (vec) gate_logits_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
+    else gate_logits_scalar_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
   } else {
     const float* xf = static_cast<const float*>(x);
-    if (vec) {
-      cudaError_t err = cudaFuncSetAttribute(gate_logits_kernel<float>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (err != cudaSuccess) return err;
-      gate_logits_kernel<float><<<grid, 128, smem, s>>>(xf, Wg, T, d, E, logits);
-    } else {
-      gate_logits_scalar_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
-    }
+    if (vec) gate_logits_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
+    else gate_logits_scalar_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
   }
   return cudaGetLastError();
 }
