@@ -2,6 +2,8 @@
 // launch sequence of each entry point.  All device work is in the kernels of this library.
 #include <math.h>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "../../include/moe.h"
 #include "launch.h"
@@ -25,6 +27,9 @@ int capacity_of(int T, int E, float cf) {
 }
 
 // ---------------------------------------------------------------- workspace layout
+// Token rows per tile of the first (gathering) GEMM.
+constexpr int kGather1Rows = 64;
+
 // Split-K applies to decode-sized batches only: at most kMaxSplit chunks, and only when the
 // expert slots plus residual rows fit in kSplitRows (the fp32 partial sums then stay small).
 constexpr int kMaxSplit = 32;
@@ -133,8 +138,42 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D f16 row-major tensor [outer, inner] with a {box_inner, box_outer} box, 128-byte swizzle.
+// A descriptor encodes only an address and a geometry, so encoded ones are kept in a small
+// per-thread cache keyed by exactly those (a layer called again with the same buffers skips
+// the encoding).
+struct MapKey {
+  const void* ptr;
+  uint64_t inner, outer;
+  uint32_t bi, bo;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && inner == o.inner && outer == o.outer && bi == o.bi && bo == o.bo;
+  }
+};
+constexpr int kMapCache = 32;
+thread_local MapKey t_map_keys[kMapCache];
+thread_local CUtensorMap t_maps[kMapCache];
+thread_local int t_map_used = 0, t_map_next = 0;
+
+bool encode_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                uint32_t box_inner, uint32_t box_outer);
+
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
               uint32_t box_outer) {
+  const MapKey key{ptr, inner, outer, box_inner, box_outer};
+  for (int i = 0; i < t_map_used; ++i)
+    if (t_map_keys[i] == key) {
+      *m = t_maps[i];
+      return true;
+    }
+  if (!encode_map(m, ptr, inner, outer, box_inner, box_outer)) return false;
+  const int slot = t_map_used < kMapCache ? t_map_used++ : (t_map_next++ % kMapCache);
+  t_map_keys[slot] = key;
+  t_maps[slot] = *m;
+  return true;
+}
+
+bool encode_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                uint32_t box_inner, uint32_t box_outer) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -230,20 +269,25 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
                       const float* slot_w, const int32_t* drop_slot_of, float* partial,
                       size_t partial_bytes, int* status, cudaStream_t s) {
   const bool residual = Wr1 != nullptr;
-  TcPlan plan;
-  if (!tc_plan(rows_bound, &plan)) return MOE_ERR_CUDA;
+  // first GEMM: tiles of at most 64 token rows, so that items can span four weight blocks and
+  // each gathered row (a tile::gather4 TMA instruction per four rows) feeds four MMAs
+  TcPlan plan1, plan2;
+  if (!tc_plan(std::min(rows_bound, kGather1Rows), &plan1) || !tc_plan(rows_bound, &plan2))
+    return MOE_ERR_CUDA;
   const int T_res = residual ? T : 0;
   const int part_rows = S_rows + T_res;
-  const long long tiles_bound = std::min(E, S_rows) + S_rows / plan.nmax;
-  const long long res_tiles = residual ? (T + plan.nmax - 1) / plan.nmax : 0;
-  const int mw1 = choose_mw(tiles_bound, f, res_tiles, f_res, plan, E);
-  const int mw2 = choose_mw(tiles_bound, d, res_tiles, d, plan, E);
+  const long long tiles1 = std::min(E, S_rows) + S_rows / plan1.nmax;
+  const long long res1 = residual ? (T + plan1.nmax - 1) / plan1.nmax : 0;
+  const long long tiles2 = std::min(E, S_rows) + S_rows / plan2.nmax;
+  const long long res2 = residual ? (T + plan2.nmax - 1) / plan2.nmax : 0;
+  const int mw1 = choose_mw(tiles1, f, res1, f_res, plan1, E);
+  const int mw2 = choose_mw(tiles2, d, res2, d, plan2, E);
   int ks1 = 1, ks2 = 1;
   if (partial) {
-    ks1 = choose_ksplit(tiles_bound * (f / 128 / mw1) + res_tiles * (residual ? f_res / 128 / mw1 : 0),
-                        d / 64, plan.grid);
-    ks2 = choose_ksplit((tiles_bound + res_tiles) * (d / 128 / mw2),
-                        residual ? std::min(f, f_res) / 64 : f / 64, plan.grid);
+    ks1 = choose_ksplit(tiles1 * (f / 128 / mw1) + res1 * (residual ? f_res / 128 / mw1 : 0),
+                        d / 64, plan1.grid);
+    ks2 = choose_ksplit((tiles2 + res2) * (d / 128 / mw2),
+                        residual ? std::min(f, f_res) / 64 : f / 64, plan2.grid);
     const size_t cols1 = std::max(f, residual ? f_res : 0);
     if ((size_t)ks1 * part_rows * cols1 * 4 > partial_bytes) ks1 = 1;
     if ((size_t)ks2 * part_rows * d * 4 > partial_bytes) ks2 = 1;
@@ -263,7 +307,7 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
     mHres = mH;
   }
   GemmArgs g1;
-  fill_common(g1, plan, E, mw1, status);
+  fill_common(g1, plan1, E, mw1, status);
   if (g1.stages < 2) return MOE_ERR_UNSUPPORTED;
   g1.offsets = offsets;
   g1.perm = perm;
@@ -292,12 +336,12 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   g1.part_rows = part_rows;
   g1.part_cols = std::max(f, residual ? f_res : 0);
   g1.part_res_row0 = S_rows;
-  MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan.grid, s));
+  MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan1.grid, s));
   if (ks1 > 1) MOE_TRY(launch_splitk_reduce1(g1, S_rows, T_res, f, f_res, s));
   MOE_TRY(stage_mark(4, s));
 
   GemmArgs g2;
-  fill_common(g2, plan, E, mw2, status);
+  fill_common(g2, plan2, E, mw2, status);
   if (g2.stages < 2) return MOE_ERR_UNSUPPORTED;
   g2.offsets = offsets;
   g2.perm = perm;
@@ -318,7 +362,7 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   g2.part_rows = part_rows;
   g2.part_cols = d;
   g2.part_res_row0 = S_rows;
-  MOE_TRY(launch_grouped_gemm2(mW2, mH, mWr2, mHres, g2, plan.grid, s));
+  MOE_TRY(launch_grouped_gemm2(mW2, mH, mWr2, mHres, g2, plan2.grid, s));
   if (ks2 > 1) MOE_TRY(launch_splitk_reduce2(g2, S_rows, T_res, d, s));
   MOE_TRY(stage_mark(5, s));
   return MOE_OK;
@@ -327,6 +371,22 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
 }  // namespace
 
 namespace moe {
+
+cudaError_t ensure_smem_attr(const void* kernel) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  int optin = 0;
+  err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (err == cudaSuccess) done.insert({kernel, dev});
+  return err;
+}
 
 // Argument checks of the allocation-free expert FFN (noalloc.cu): those of moe_expert_ffn
 // without the workspace.

@@ -238,7 +238,7 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C,
   if (stage_out) smem = staged;
   const bool in_regs = (n + kWarps - 1) / kWarps <= 32 * kRegBatches;
   auto kern = in_regs ? dispatch_kernel<kRegBatches> : dispatch_kernel<0>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern));
   if (err != cudaSuccess) return err;
   kern<<<1, kWarps * 32, smem, s>>>(topk_idx, n, k, E, C, counts_raw, kept, offsets,
                                     perm, slot_of, topk_w, slot_w, S_cap, stage_out);

@@ -190,6 +190,86 @@ __global__ void __launch_bounds__(256) gate_logits_scalar_kernel(const Tin* __re
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Small batches (T <= 64): one thread per (token, expert) chain.  Block = 8 tokens (warps) x
+// 32 experts (lanes); raw Wg and token chunks stream through a four-deep cp.async ring, so
+// the cost is close to the d dependent multiply-adds of one chain instead of a 64-token tile.
+constexpr int kSKC = 64;       // shared-dimension chunk
+constexpr int kSStages = 4;    // ring depth
+constexpr int kSTok = 8;       // tokens per block (one per warp)
+constexpr int kSExp = 32;      // experts per block (one per lane)
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <typename Tin>
+__host__ __device__ constexpr size_t small_slot_bytes() {
+  return (size_t)kSKC * kSExp * sizeof(float) + (size_t)kSTok * kSKC * sizeof(Tin);
+}
+
+// Needs d % 64 == 0, E % 4 == 0, 16-byte aligned rows.
+template <typename Tin>
+__global__ void __launch_bounds__(256) gate_logits_small_kernel(const Tin* __restrict__ x,
+                                                                const float* __restrict__ Wg,
+                                                                int T, int d, int E,
+                                                                float* __restrict__ logits) {
+  extern __shared__ __align__(16) uint8_t ssm[];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int e0 = blockIdx.x * kSExp, t0 = blockIdx.y * kSTok;
+  const int nch = d / kSKC;
+  constexpr size_t slot = small_slot_bytes<Tin>();
+  auto issue = [&](int c) {
+    uint8_t* base = ssm + (size_t)(c % kSStages) * slot;
+    const int k0 = c * kSKC;
+    // Wg rows k0 .. k0+63, experts e0 .. e0+31: 64 x 8 pieces of 16 bytes
+    for (int q = threadIdx.x; q < kSKC * (kSExp / 4); q += 256) {
+      const int row = q >> 3, col = (q & 7) * 4;
+      const int e = e0 + col;
+      cp_async16(base + (row * kSExp + col) * 4, Wg + (size_t)(k0 + row) * E + min(e, E - 4),
+                 e < E ? 16 : 0);
+    }
+    // tokens t0 .. t0+7, columns k0 .. k0+63
+    constexpr int kPer = 16 / (int)sizeof(Tin);
+    uint8_t* xb = base + (size_t)kSKC * kSExp * 4;
+    for (int q = threadIdx.x; q < kSTok * (kSKC / kPer); q += 256) {
+      const int tt = q / (kSKC / kPer), col = (q % (kSKC / kPer)) * kPer;
+      const int t = t0 + tt;
+      cp_async16(xb + (tt * kSKC + col) * sizeof(Tin), x + (size_t)min(t, T - 1) * d + k0 + col,
+                 t < T ? 16 : 0);
+    }
+  };
+#pragma unroll
+  for (int c = 0; c < kSStages - 1; ++c) {
+    if (c < nch) issue(c);
+    cp_async_commit();
+  }
+  float acc = 0.0f;
+  for (int c = 0; c < nch; ++c) {
+    if (c + kSStages - 1 < nch) issue(c + kSStages - 1);
+    cp_async_commit();
+    cp_async_wait<kSStages - 1>();
+    __syncthreads();
+    const uint8_t* base = ssm + (size_t)(c % kSStages) * slot;
+    const float* ws = reinterpret_cast<const float*>(base);
+    const Tin* xs = reinterpret_cast<const Tin*>(base + (size_t)kSKC * kSExp * 4) + w * kSKC;
+#pragma unroll 16
+    for (int kk = 0; kk < kSKC; ++kk)            // ascending i
+      acc = __fmaf_rn(to_f32<Tin>(xs[kk]), ws[kk * kSExp + lane], acc);
+    __syncthreads();                             // the slot may be refilled next
+  }
+  cp_async_wait<0>();
+  const int t = t0 + w, e = e0 + lane;
+  if (t < T && e < E) logits[(size_t)t * E + e] = acc;
+}
+
 // (v, i) beats (w, j) when v > w, or v == w and i < j: descending logit, ties to lower index.
 __device__ __forceinline__ bool beats(float v, int i, float w, int j) {
   return v > w || (v == w && i < j);
@@ -259,6 +339,21 @@ __global__ void __launch_bounds__(256) softmax_topk_kernel(const float* __restri
 
 cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, int T, int d, int E,
                                float* logits, cudaStream_t s) {
+  const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+                       (reinterpret_cast<uintptr_t>(Wg) & 15) == 0;
+  if (T <= 64 && d % kSKC == 0 && E % 4 == 0 && aligned) {
+    dim3 g((E + kSExp - 1) / kSExp, (T + kSTok - 1) / kSTok);
+    if (dtype_f16) {
+      const size_t smem = kSStages * small_slot_bytes<__half>();
+      gate_logits_small_kernel<__half><<<g, 256, smem, s>>>(static_cast<const __half*>(x), Wg, T, d,
+                                                            E, logits);
+    } else {
+      const size_t smem = kSStages * small_slot_bytes<float>();
+      gate_logits_small_kernel<float><<<g, 256, smem, s>>>(static_cast<const float*>(x), Wg, T, d, E,
+                                                           logits);
+    }
+    return cudaGetLastError();
+  }
   dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);
   const bool vec = d % 8 == 0 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(Wg) & 15) == 0 &&

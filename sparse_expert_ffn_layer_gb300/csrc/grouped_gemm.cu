@@ -408,8 +408,7 @@ template <bool G, int Epi, int MW>
 cudaError_t launch_mw(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                       const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s) {
   const SmemLayout L = smem_layout(args.nmax, args.stages, args.E, MW);
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<G, Epi, MW>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_kernel<G, Epi, MW>));
   if (err != cudaSuccess) return err;
   grouped_gemm_kernel<G, Epi, MW><<<grid, kThreads, L.total, s>>>(A, B, Ar, Br, args);
   return cudaGetLastError();

@@ -71,6 +71,9 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C,
                             int32_t* slot_of, const float* topk_w, float* slot_w, cudaStream_t s);
 
 int gemm_stages_for(int nmax, int E, int mw, int smem_limit);
+// Raises the kernel's dynamic shared-memory limit to the device maximum, once per kernel
+// and device (host side; launches of any size up to that maximum then need no further call).
+cudaError_t ensure_smem_attr(const void* kernel);
 cudaError_t launch_grouped_gemm1(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                                  const CUtensorMap& Br, const GemmArgs& args, int grid,
                                  cudaStream_t s);
