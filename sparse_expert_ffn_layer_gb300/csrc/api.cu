@@ -251,8 +251,16 @@ void fill_common(GemmArgs& g, const TcPlan& p, int E, int mw, int* status) {
 thread_local cudaEvent_t* t_stage_events = nullptr;
 thread_local cudaEvent_t t_stage_store[MOE_STAGE_EVENTS];
 
+// Inside a stream capture the events are recorded as external event nodes, so that each
+// replay of the graph records them (a plain record would only order the capture).
 cudaError_t stage_mark(int i, cudaStream_t s) {
-  return t_stage_events ? cudaEventRecord(t_stage_events[i], s) : cudaSuccess;
+  if (!t_stage_events) return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t err = cudaStreamIsCapturing(s, &cs);
+  if (err != cudaSuccess) return err;
+  return cudaEventRecordWithFlags(t_stage_events[i], s,
+                                  cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                      : cudaEventRecordDefault);
 }
 
 #define MOE_TRY(expr)                          \
