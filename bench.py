@@ -45,6 +45,8 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="moe350m_e128")
     p.add_argument("--tokens", type=int, default=4096)
+    p.add_argument("--experts", type=int, default=None,
+                   help="override the workload's expert count (smaller profiling cases)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=20.0)
@@ -235,7 +237,10 @@ def count_graph_kernels(g):
             path = os.path.join(tmp, "step.dot")
             g.debug_dump(path)
             text = open(path).read()
-        names = [ln for ln in text.splitlines() if "KERNEL" in ln and "label" in ln]
+        if os.environ.get("MOE_BENCH_DUMP_GRAPH"):
+            with open(os.environ["MOE_BENCH_DUMP_GRAPH"], "w") as fh:
+                fh.write(text)
+        names = [ln for ln in text.splitlines() if "KERNEL" in ln.upper() and "->" not in ln]
         return len(names) or None
     except Exception:
         return None
@@ -255,6 +260,8 @@ def run_ours(args):
         dist.init_process_group("nccl")
 
     cfg, T = synth.workload(args.workload, args.tokens)
+    if args.experts:
+        cfg = cfg.at(E=args.experts)
     seed = args.seed + 1000 * rank
     f16 = cfg.dtype == "f16"
     tdt = torch.float16 if f16 else torch.float32
@@ -313,26 +320,27 @@ def run_ours(args):
     for ev_step in evs:                  # torch creates the CUDA event at its first record
         for ev in ev_step:
             ev.record(stream)
-    # Each timed step is one moe_layer_forward call.  By default every step is captured
-    # into its own CUDA graph first (with its stage events) and the K graphs are replayed
-    # back to back, so the device timing is not limited by host-side launch cost at small T.
-    graphs = []
-    kernels_per_step = None
-    if not args.no_graph:
-        cap_stream = torch.cuda.Stream()
-        torch.cuda.synchronize()
-        for i in range(K):
-            g = torch.cuda.CUDAGraph()
-            if i == 0 and hasattr(g, "enable_debug_mode"):
-                g.enable_debug_mode()
-            with torch.cuda.graph(g, stream=cap_stream):
-                moe.moe_set_stage_events(evs[i])
-                step(dev_tok[i % n_batches])
-            moe.moe_set_stage_events(None)
-            if i == 0:
-                kernels_per_step = count_graph_kernels(g)
-            graphs.append(g)
-        torch.cuda.synchronize()
+    # Each timed step is one moe_layer_forward call.  By default the call is captured into a
+    # CUDA graph per token batch and the graphs are replayed back to back, so the device
+    # timing is not limited by host-side launch cost at small T.  The timed region carries
+    # no stage events (each event record costs about a microsecond); a second pass of K
+    # steps, each captured with its own stage events, times the stages and the dominant
+    # kernel.
+    cap_stream = torch.cuda.Stream()
+
+    def capture(batch, events=None, debug=False):
+        g = torch.cuda.CUDAGraph()
+        if debug and hasattr(g, "enable_debug_mode"):
+            g.enable_debug_mode()
+        with torch.cuda.graph(g, stream=cap_stream):
+            if events is not None:
+                moe.moe_set_stage_events(events)
+            step(dev_tok[batch])
+        moe.moe_set_stage_events(None)
+        return g
+
+    plain = [] if args.no_graph else [capture(b, debug=(b == 0)) for b in range(n_batches)]
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     props = torch.cuda.get_device_properties(local)
     uuid = getattr(props, "uuid", None)
@@ -346,15 +354,13 @@ def run_ours(args):
     t_wall0 = time.time()
     e0.record(stream)
     for i in range(K):
-        if graphs:
-            graphs[i].replay()
+        if plain:
+            plain[i % n_batches].replay()
         else:
-            moe.moe_set_stage_events(evs[i])
             step(dev_tok[i % n_batches])
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
-    moe.moe_set_stage_events(None)
     if world > 1:
         dist.barrier()
     clocks.stop()
@@ -362,26 +368,27 @@ def run_ours(args):
     if status != moe.MOE_OK:
         raise RuntimeError(f"device status {moe.moe_status_string(status)}")
     ms = e0.elapsed_time(e1)
-    stage_source = "timed region"
 
-    def stage_times():
-        acc = np.zeros(moe.MOE_STAGE_EVENTS - 1)
-        for i in range(K):
-            for j in range(moe.MOE_STAGE_EVENTS - 1):
-                acc[j] += evs[i][j].elapsed_time(evs[i][j + 1])
-        return acc / K
-
-    try:
-        stage_ms = stage_times()
-    except Exception:
-        # events inside graphs could not be timed: time the stages over K direct calls
-        stage_source = "separate pass of direct calls"
+    # stage pass: the same K steps, each with its own stage events
+    if args.no_graph:
         for i in range(K):
             moe.moe_set_stage_events(evs[i])
             step(dev_tok[i % n_batches])
         moe.moe_set_stage_events(None)
+        stage_source = "second pass of K direct calls with stage events"
+    else:
+        staged = [capture(i % n_batches, evs[i]) for i in range(K)]
         torch.cuda.synchronize()
-        stage_ms = stage_times()
+        for g in staged:
+            g.replay()
+        stage_source = "second pass of K graph replays with stage events"
+    torch.cuda.synchronize()
+    stage_ms = np.zeros(moe.MOE_STAGE_EVENTS - 1)
+    for i in range(K):
+        for j in range(moe.MOE_STAGE_EVENTS - 1):
+            stage_ms[j] += evs[i][j].elapsed_time(evs[i][j + 1])
+    stage_ms /= K
+    kernels_per_step = count_graph_kernels(plain[0]) if plain else None
 
     # end to end through the public API with host buffers: H2D tokens, forward, D2H output
     h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
