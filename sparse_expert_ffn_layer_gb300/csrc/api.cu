@@ -201,20 +201,28 @@ bool tc_plan(int rows_bound, TcPlan* p) {
   Dev dv;
   if (!dev_props(&dv)) return false;
   p->nmax = std::min(256, std::max(16, (rows_bound + 15) / 16 * 16));
-  p->acc_cols = pow2_at_least((uint32_t)p->nmax);
+  p->acc_cols = (uint32_t)((p->nmax + 31) / 32 * 32);
   p->grid = dv.sms;
   p->smem_optin = dv.smem_optin;
   return true;
 }
 
+// Accumulator sets that fit TMEM (512 columns) for mw blocks: 2 (the epilogue overlaps the
+// next item's MMAs), else 1, else 0 (does not fit).
+int nbuf_for(int mw, uint32_t acc_cols) {
+  if (2u * (uint32_t)mw * acc_cols <= 512u) return 2;
+  if ((uint32_t)mw * acc_cols <= 512u) return 1;
+  return 0;
+}
+
 // Weight blocks per item of one GEMM (1, 2 or 4 adjacent 128-row blocks sharing one gather of
-// the token rows): the widest that divides every group's M, fits TMEM (two buffers) and
-// three pipeline stages, and still leaves about six waves of items.
+// the token rows): the widest that divides every group's M, fits TMEM and three pipeline
+// stages, and still leaves about six waves of items.
 int choose_mw(long long row_tiles, int M_exp, long long res_tiles, int M_res, const TcPlan& p,
               int E) {
   for (int mw = 4; mw >= 2; mw /= 2) {
     if (M_exp % (128 * mw) || (res_tiles && M_res % (128 * mw))) continue;
-    if (2u * (uint32_t)mw * p.acc_cols > 512u) continue;
+    if (nbuf_for(mw, p.acc_cols) == 0) continue;
     if (gemm_stages_for(p.nmax, E, mw, p.smem_optin) < 3) continue;
     const long long items = row_tiles * (M_exp / (128 * mw)) + res_tiles * (M_res / (128 * mw));
     if (items >= 6LL * p.grid) return mw;
@@ -241,6 +249,8 @@ void fill_common(GemmArgs& g, const TcPlan& p, int E, int mw, int* status) {
   g.mw = mw;
   g.stages = gemm_stages_for(p.nmax, E, mw, p.smem_optin);
   g.acc_cols = p.acc_cols;
+  g.nbuf = nbuf_for(mw, p.acc_cols);
+  g.tmem_cols = pow2_at_least((uint32_t)g.nbuf * (uint32_t)mw * p.acc_cols);
   g.a_lbo = kALbo;
   g.a_sbo = kASbo;
   g.status = status;

@@ -64,30 +64,34 @@ struct Tile {
 // Maps work item i to its tile.  prefix[e] = chunks of experts < e (prefix[E] = total).
 __device__ __forceinline__ Tile decode(int i, const GemmArgs& a, const int32_t* prefix,
                                        const int32_t* offs) {
+  // Items of one group are ordered weight block major, row tile minor, so the row tiles that
+  // read the same weight block run side by side on neighbouring CTAs and share it in L2.
   Tile t;
   const int n_exp = prefix[a.E] * a.mt_exp;
   if (i < n_exp) {
-    const int j = i / a.mt_exp;
-    t.mt = i - j * a.mt_exp;
-    int lo = 0, hi = a.E;                   // largest e with prefix[e] <= j
+    int lo = 0, hi = a.E;                   // largest e with prefix[e] * mt_exp <= i
     while (hi - lo > 1) {
       int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= j) lo = mid; else hi = mid;
+      if (prefix[mid] * a.mt_exp <= i) lo = mid; else hi = mid;
     }
+    const int chunks = prefix[lo + 1] - prefix[lo];
+    const int local = i - prefix[lo] * a.mt_exp;
+    t.mt = local / chunks;
+    const int chunk = local - t.mt * chunks;
     t.res = 0;
     t.e = lo;
-    const int chunk = j - prefix[lo];
     const int kept = offs[lo + 1] - offs[lo];
     t.row0 = offs[lo] + chunk * a.nmax;
     t.n = min(a.nmax, kept - chunk * a.nmax);
     t.K = a.K;
   } else {
-    const int q = i - n_exp;
-    const int j = q / a.mt_res;
-    t.mt = q - j * a.mt_res;
+    const int chunks = (a.n_res_rows + a.nmax - 1) / a.nmax;
+    const int local = i - n_exp;
+    t.mt = local / chunks;
+    const int chunk = local - t.mt * chunks;
     t.res = 1;
     t.e = 0;
-    t.row0 = j * a.nmax;
+    t.row0 = chunk * a.nmax;
     t.n = min(a.nmax, a.n_res_rows - t.row0);
     t.K = a.K_res;
   }
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmB_res);
     }
   }
-  if (warp == 1) tmem_alloc(tmem_holder, 2 * mw * a.acc_cols);
+  if (warp == 1) tmem_alloc(tmem_holder, a.tmem_cols);
   // chunk prefix over experts (warp 2), E <= 1024
   if (warp == 2) {
     for (int e = lane; e <= a.E; e += 32) soffs[e] = a.offsets[e];
@@ -258,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile t = decode(i / ksplit, a, prefix, soffs);
       const int ks = i - (i / ksplit) * ksplit;
       const int npad = max(16, (t.n + 15) & ~15);
-      const int buf = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1) & 1u;
+      const int buf = local % a.nbuf;
+      const uint32_t use = (uint32_t)(local / a.nbuf) & 1u;
       bool ok = true;
       if (lane == 0) ok = mbar_wait_bounded(&acc_empty[buf], use ^ 1u, abort_flag, a.status, a.wait_ns);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -325,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++local) {
       const Tile t = decode(i / ksplit, a, prefix, soffs);
       const int ks = i - (i / ksplit) * ksplit;
-      const int buf = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1) & 1u;
+      const int buf = local % a.nbuf;
+      const uint32_t use = (uint32_t)(local / a.nbuf) & 1u;
       // second GEMM: each warp stages the tile's tokens and gate weights in its own shared
       // memory while the accumulator is still being computed (a load per row per warp
       // instead of one per row per thread; warp-private, so no cross-warp barrier)
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, 2 * mw * a.acc_cols);
+  if (warp == 1) tmem_dealloc(tmem_base, a.tmem_cols);
 }
 
 template <bool G, int Epi, int MW>

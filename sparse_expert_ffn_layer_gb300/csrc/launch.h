@@ -27,7 +27,9 @@ struct GemmArgs {
   int a_rows_per_expert;    // rows of the A tensor map per expert
   int nmax;                 // rows per tile, multiple of 16, <= 256
   int stages;               // pipeline depth
-  uint32_t acc_cols;        // TMEM columns per accumulator buffer (power of two >= 32)
+  uint32_t acc_cols;        // TMEM columns per accumulator (nmax rounded up to 32)
+  int nbuf;                 // accumulator sets (2: the epilogue overlaps the next item)
+  uint32_t tmem_cols;       // TMEM columns allocated: power of two >= nbuf * mw * acc_cols
   uint32_t a_lbo, a_sbo;    // A (M-major, 128-byte swizzle) descriptor byte offsets
   int mode;                 // kMode* (second GEMM)
   // first GEMM outputs
