@@ -13,21 +13,26 @@ namespace {
 constexpr int kTT = 64;   // tokens per block tile
 constexpr int kTE = 64;   // experts per block tile
 constexpr int kKC = 32;   // shared-dimension chunk staged in shared memory
-constexpr int kXP = kKC + 4;  // padded row of the token tile (16-byte aligned rows)
+constexpr int kVKC = 64;           // shared-dimension chunk of the vector kernel
+constexpr int kXT = kTT + 4;       // padded row of the i-major token tile
 
+// One thread's share of a 64-token x 64 chunk of the tokens: 16 consecutive values of a row.
 template <typename Tin>
-struct XChunk;  // one thread's share of a 64 x 32 token chunk: 8 consecutive values of a row
+struct XChunk;
 
 template <>
 struct XChunk<__half> {
-  uint4 raw;
-  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint4*>(p); }
-  __device__ __forceinline__ void zero() { raw = make_uint4(0u, 0u, 0u, 0u); }
-  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
-    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+  uint4 raw[2];
+  __device__ __forceinline__ void load(const __half* p) {
+    raw[0] = *reinterpret_cast<const uint4*>(p);
+    raw[1] = *reinterpret_cast<const uint4*>(p + 8);
+  }
+  __device__ __forceinline__ void zero() { raw[0] = raw[1] = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ void to_f32(float (&v)[16]) const {
+    const __half2* h = reinterpret_cast<const __half2*>(raw);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float2 f = __half22float2(h[q]);      // exact widening
+    for (int q = 0; q < 8; ++q) {
+      const float2 f = __half22float2(h[q]);      // exact widening
       v[2 * q] = f.x;
       v[2 * q + 1] = f.y;
     }
@@ -36,31 +41,45 @@ struct XChunk<__half> {
 
 template <>
 struct XChunk<float> {
-  float4 a, b;
+  float4 r[4];
   __device__ __forceinline__ void load(const float* p) {
-    a = *reinterpret_cast<const float4*>(p);
-    b = *reinterpret_cast<const float4*>(p + 4);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) r[q] = *reinterpret_cast<const float4*>(p + 4 * q);
   }
-  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
-  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) r[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __device__ __forceinline__ void to_f32(float (&v)[16]) const {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[4 * q] = r[q].x; v[4 * q + 1] = r[q].y; v[4 * q + 2] = r[q].z; v[4 * q + 3] = r[q].w;
+    }
   }
 };
 
-// logits[T, E] = x[T, d] . Wg[d, E]; 256 threads, 4 x 4 outputs per thread.  The next chunk
-// is fetched into registers while the current one is multiplied (double-buffered tiles).
-// Vector path: d % 8 == 0 and E % 4 == 0 (16-byte loads); otherwise the scalar kernel below.
+size_t gate_vec_smem_bytes() { return sizeof(float) * 2 * kVKC * (kXT + kTE); }
+
+// logits[T, E] = x[T, d] . Wg[d, E] for larger batches: 256 threads on a 64-token x 64-expert
+// tile, 4 tokens x 4 experts per thread.  A warp spans 8 token groups x 4 expert groups, so
+// each step i reads 128 bytes of tokens and 64 bytes of gate weights per warp (two
+// shared-memory wavefronts for 16 multiply-adds per thread) and the kernel stays bound by
+// the FP32 pipe.  The token tile is stored i-major and widened to fp32; 64-wide chunks are
+// fetched into registers one chunk ahead.  Needs d % 16 == 0 and E % 4 == 0.
 template <typename Tin>
 __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict__ x,
                                                           const float* __restrict__ Wg, int T,
                                                           int d, int E,
                                                           float* __restrict__ logits) {
-  __shared__ __align__(16) float xs[2][kTT][kXP];   // token tile: xs[t][i]
-  __shared__ __align__(16) float ws[2][kKC][kTE];   // Wg tile: ws[i][e]
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  extern __shared__ __align__(16) float gsm[];
+  float (*xs)[kVKC][kXT] = reinterpret_cast<float (*)[kVKC][kXT]>(gsm);                 // [2]
+  float (*ws)[kVKC][kTE] = reinterpret_cast<float (*)[kVKC][kTE]>(gsm + 2 * kVKC * kXT);  // [2]
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int tg = (wp & 1) * 8 + (lane & 7);        // token group: tokens 4 tg .. 4 tg + 3
+  const int eg = (wp >> 1) * 4 + (lane >> 3);      // expert group: experts 4 eg .. 4 eg + 3
   const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
-  // loader roles: token row lt, columns lk .. lk+7; Wg rows lw, lw+16 (4 experts at le)
-  const int lt = threadIdx.x >> 2, lk = (threadIdx.x & 3) * 8;
+  // loader roles: token row lt, columns lk .. lk+15; Wg rows lw + 16 r, experts le .. le+3
+  const int lt = threadIdx.x >> 2, lk = (threadIdx.x & 3) * 16;
   const int lw = threadIdx.x >> 4, le = (threadIdx.x & 15) * 4;
   float acc[4][4];
 #pragma unroll
@@ -69,47 +88,50 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
 
   XChunk<Tin> xr;
-  float4 wr0, wr1;
+  float4 wr[4];
   auto fetch = [&](int k0) {
     const int t = t0 + lt;
-    const int kc = min(kKC, d - k0);
+    const int kc = min(kVKC, d - k0);
     if (t < T && lk < kc) xr.load(x + (size_t)t * d + k0 + lk);
     else xr.zero();
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     const bool eok = e0 + le < E;
-    wr0 = (eok && lw < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw) * E + e0 + le) : z;
-    wr1 = (eok && lw + 16 < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw + 16) * E + e0 + le) : z;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int row = lw + 16 * r;
+      wr[r] = (eok && row < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + row) * E + e0 + le)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   };
   auto stash = [&](int buf) {
-    float v[8];
+    float v[16];
     xr.to_f32(v);
-    *reinterpret_cast<float4*>(&xs[buf][lt][lk]) = make_float4(v[0], v[1], v[2], v[3]);
-    *reinterpret_cast<float4*>(&xs[buf][lt][lk + 4]) = make_float4(v[4], v[5], v[6], v[7]);
-    *reinterpret_cast<float4*>(&ws[buf][lw][le]) = wr0;
-    *reinterpret_cast<float4*>(&ws[buf][lw + 16][le]) = wr1;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) xs[buf][lk + j][lt] = v[j];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) *reinterpret_cast<float4*>(&ws[buf][lw + 16 * r][le]) = wr[r];
   };
 
   fetch(0);
   stash(0);
   __syncthreads();
   int buf = 0;
-  for (int k0 = 0; k0 < d; k0 += kKC) {
-    const int kc = min(kKC, d - k0);
-    const bool more = k0 + kKC < d;
-    if (more) fetch(k0 + kKC);
+  for (int k0 = 0; k0 < d; k0 += kVKC) {
+    const int kc = min(kVKC, d - k0);
+    const bool more = k0 + kVKC < d;
+    if (more) fetch(k0 + kVKC);
     auto step = [&](int kk) {                      // one i: 16 chained multiply-adds
-      const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][tx * 4]);
-      const float av[4] = {xs[buf][ty * 4][kk], xs[buf][ty * 4 + 1][kk], xs[buf][ty * 4 + 2][kk],
-                           xs[buf][ty * 4 + 3][kk]};
+      const float4 a = *reinterpret_cast<const float4*>(&xs[buf][kk][tg * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][eg * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
       const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
     };
-    if (kc == kKC) {                               // full chunk: straight-line code
+    if (kc == kVKC) {                              // full chunk: straight-line code
 #pragma unroll
-      for (int kk = 0; kk < kKC; ++kk) step(kk);   // ascending i
+      for (int kk = 0; kk < kVKC; ++kk) step(kk);  // ascending i
     } else {
       for (int kk = 0; kk < kc; ++kk) step(kk);    // ascending i, no padding steps
     }
@@ -119,9 +141,9 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
+    const int t = t0 + tg * 4 + i;
     if (t >= T) continue;
-    const int e = e0 + tx * 4;
+    const int e = e0 + eg * 4;
     if (e + 3 < E) {
       *reinterpret_cast<float4*>(logits + (size_t)t * E + e) =
           make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
@@ -355,17 +377,28 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
     return cudaGetLastError();
   }
   dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);
-  const bool vec = d % 8 == 0 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+  const bool vec = d % 16 == 0 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(Wg) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+  const size_t vsmem = gate_vec_smem_bytes();
   if (dtype_f16) {
     const __half* xh = static_cast<const __half*>(x);
-    if (vec) gate_logits_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
-    else gate_logits_scalar_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
+    if (vec) {
+      cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(gate_logits_kernel<__half>));
+      if (err != cudaSuccess) return err;
+      gate_logits_kernel<__half><<<grid, 256, vsmem, s>>>(xh, Wg, T, d, E, logits);
+    } else {
+      gate_logits_scalar_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
+    }
   } else {
     const float* xf = static_cast<const float*>(x);
-    if (vec) gate_logits_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
-    else gate_logits_scalar_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
+    if (vec) {
+      cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(gate_logits_kernel<float>));
+      if (err != cudaSuccess) return err;
+      gate_logits_kernel<float><<<grid, 256, vsmem, s>>>(xf, Wg, T, d, E, logits);
+    } else {
+      gate_logits_scalar_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
+    }
   }
   return cudaGetLastError();
 }
