@@ -119,6 +119,9 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
     const int kc = min(kVKC, d - k0);
     const bool more = k0 + kVKC < d;
     if (more) fetch(k0 + kVKC);
+    // keep the prefetch loads above the multiply-adds: without this fence the compiler may
+    // sink them to their first use after the loop and serialise their latency with the math
+    asm volatile("" ::: "memory");
     auto step = [&](int kk) {                      // one i: 16 chained multiply-adds
       const float4 a = *reinterpret_cast<const float4*>(&xs[buf][kk][tg * 4]);
       const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][eg * 4]);
