@@ -295,6 +295,101 @@ __global__ void __launch_bounds__(256) gate_logits_small_kernel(const Tin* __res
   if (t < T && e < E) logits[(size_t)t * E + e] = acc;
 }
 
+// ---------------------------------------------------------------------------------------
+// Larger batches (f16 tokens): lane = token, 16 experts per thread.  Block = 8 warps over
+// 32 tokens x 128 experts.  Each step i reads the 16 gate weights of a warp's experts with
+// four warp-uniform (broadcast) 16-byte shared loads and takes the lane's token value from
+// registers, so one shared-memory wavefront feeds four multiply-add instructions.  Raw token
+// and Wg chunks stream through a three-deep cp.async ring.  Needs f16 tokens, d % 64 == 0,
+// E % 16 == 0, 16-byte aligned rows.
+constexpr int kLTok = 32;        // tokens per block (one per lane)
+constexpr int kLExp = 128;       // experts per block (16 per warp)
+constexpr int kLKC = 64;         // shared-dimension chunk
+constexpr int kLStages = 3;      // ring depth
+constexpr int kLXRow = kLKC + 8; // padded row (halves) of the raw token chunk
+
+__host__ __device__ constexpr size_t lane_slot_bytes() {
+  return (size_t)kLKC * kLExp * sizeof(float) + (size_t)kLTok * kLXRow * sizeof(__half);
+}
+
+__global__ void __launch_bounds__(256) gate_logits_lane_kernel(const __half* __restrict__ x,
+                                                               const float* __restrict__ Wg,
+                                                               int T, int d, int E,
+                                                               float* __restrict__ logits) {
+  extern __shared__ __align__(16) uint8_t lsm[];
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * kLTok, e0 = blockIdx.y * kLExp;
+  const int nch = d / kLKC;
+  constexpr size_t slot = lane_slot_bytes();
+  auto issue = [&](int c) {
+    uint8_t* base = lsm + (size_t)(c % kLStages) * slot;
+    const int k0 = c * kLKC;
+    // Wg rows k0 .. k0+63, experts e0 .. e0+127: 64 x 32 pieces of 16 bytes
+    for (int q = threadIdx.x; q < kLKC * (kLExp / 4); q += 256) {
+      const int row = q >> 5, col = (q & 31) * 4;
+      const int e = e0 + col;
+      cp_async16(base + ((size_t)row * kLExp + col) * 4, Wg + (size_t)(k0 + row) * E + min(e, E - 4),
+                 e < E ? 16 : 0);
+    }
+    // tokens t0 .. t0+31, columns k0 .. k0+63: 32 x 8 pieces
+    __half* xb = reinterpret_cast<__half*>(base + (size_t)kLKC * kLExp * 4);
+    {
+      const int q = threadIdx.x;                 // 256 pieces, one each
+      const int tt = q >> 3, col = (q & 7) * 8;
+      const int t = t0 + tt;
+      cp_async16(xb + tt * kLXRow + col, x + (size_t)min(t, T - 1) * d + k0 + col, t < T ? 16 : 0);
+    }
+  };
+#pragma unroll
+  for (int c = 0; c < kLStages - 1; ++c) {
+    if (c < nch) issue(c);
+    cp_async_commit();
+  }
+  float acc[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+  for (int c = 0; c < nch; ++c) {
+    if (c + kLStages - 1 < nch) issue(c + kLStages - 1);
+    cp_async_commit();
+    cp_async_wait<kLStages - 1>();
+    __syncthreads();
+    const uint8_t* base = lsm + (size_t)(c % kLStages) * slot;
+    const float* ws = reinterpret_cast<const float*>(base) + wp * 16;
+    const __half* xrow = reinterpret_cast<const __half*>(base + (size_t)kLKC * kLExp * 4) + lane * kLXRow;
+    __half2 xv[kLKC / 2];
+#pragma unroll
+    for (int q = 0; q < kLKC / 8; ++q) {
+      const uint4 u = *reinterpret_cast<const uint4*>(xrow + 8 * q);
+      const __half2* h = reinterpret_cast<const __half2*>(&u);
+      xv[4 * q] = h[0]; xv[4 * q + 1] = h[1]; xv[4 * q + 2] = h[2]; xv[4 * q + 3] = h[3];
+    }
+#pragma unroll
+    for (int kk = 0; kk < kLKC; ++kk) {           // ascending i
+      const float xi = (kk & 1) ? __high2float(xv[kk >> 1]) : __low2float(xv[kk >> 1]);
+      const float4* wr = reinterpret_cast<const float4*>(ws + (size_t)kk * kLExp);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 w4 = wr[q];                  // same address in every lane: a broadcast
+        acc[4 * q] = __fmaf_rn(xi, w4.x, acc[4 * q]);
+        acc[4 * q + 1] = __fmaf_rn(xi, w4.y, acc[4 * q + 1]);
+        acc[4 * q + 2] = __fmaf_rn(xi, w4.z, acc[4 * q + 2]);
+        acc[4 * q + 3] = __fmaf_rn(xi, w4.w, acc[4 * q + 3]);
+      }
+    }
+    __syncthreads();                               // the slot may be refilled next
+  }
+  cp_async_wait<0>();
+  const int t = t0 + lane;
+  if (t < T) {
+    const int e = e0 + wp * 16;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (e + 4 * q + 3 < E)
+        *reinterpret_cast<float4*>(logits + (size_t)t * E + e + 4 * q) =
+            make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+  }
+}
+
 // (v, i) beats (w, j) when v > w, or v == w and i < j: descending logit, ties to lower index.
 __device__ __forceinline__ bool beats(float v, int i, float w, int j) {
   return v > w || (v == w && i < j);
@@ -377,6 +472,14 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
       gate_logits_small_kernel<float><<<g, 256, smem, s>>>(static_cast<const float*>(x), Wg, T, d, E,
                                                            logits);
     }
+    return cudaGetLastError();
+  }
+  if (dtype_f16 && d % kLKC == 0 && E % 16 == 0 && aligned) {
+    cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(gate_logits_lane_kernel));
+    if (err != cudaSuccess) return err;
+    dim3 g((T + kLTok - 1) / kLTok, (E + kLExp - 1) / kLExp);
+    gate_logits_lane_kernel<<<g, 256, kLStages * lane_slot_bytes(), s>>>(
+        static_cast<const __half*>(x), Wg, T, d, E, logits);
     return cudaGetLastError();
   }
   dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);
