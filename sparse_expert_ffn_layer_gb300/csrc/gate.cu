@@ -13,26 +13,21 @@ namespace {
 constexpr int kTT = 64;   // tokens per block tile
 constexpr int kTE = 64;   // experts per block tile
 constexpr int kKC = 32;   // shared-dimension chunk staged in shared memory
-constexpr int kVKC = 64;           // shared-dimension chunk of the vector kernel
-constexpr int kXT = kTT + 4;       // padded row of the i-major token tile
+constexpr int kXP = kKC + 4;  // padded row of the token tile (16-byte aligned rows)
 
-// One thread's share of a 64-token x 64 chunk of the tokens: 16 consecutive values of a row.
 template <typename Tin>
-struct XChunk;
+struct XChunk;  // one thread's share of a 64 x 32 token chunk: 8 consecutive values of a row
 
 template <>
 struct XChunk<__half> {
-  uint4 raw[2];
-  __device__ __forceinline__ void load(const __half* p) {
-    raw[0] = *reinterpret_cast<const uint4*>(p);
-    raw[1] = *reinterpret_cast<const uint4*>(p + 8);
-  }
-  __device__ __forceinline__ void zero() { raw[0] = raw[1] = make_uint4(0u, 0u, 0u, 0u); }
-  __device__ __forceinline__ void to_f32(float (&v)[16]) const {
-    const __half2* h = reinterpret_cast<const __half2*>(raw);
+  uint4 raw;
+  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void zero() { raw = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
+    const __half2* h = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float2 f = __half22float2(h[q]);      // exact widening
+    for (int q = 0; q < 4; ++q) {
+      float2 f = __half22float2(h[q]);      // exact widening
       v[2 * q] = f.x;
       v[2 * q + 1] = f.y;
     }
@@ -41,45 +36,31 @@ struct XChunk<__half> {
 
 template <>
 struct XChunk<float> {
-  float4 r[4];
+  float4 a, b;
   __device__ __forceinline__ void load(const float* p) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) r[q] = *reinterpret_cast<const float4*>(p + 4 * q);
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 4);
   }
-  __device__ __forceinline__ void zero() {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) r[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  __device__ __forceinline__ void to_f32(float (&v)[16]) const {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v[4 * q] = r[q].x; v[4 * q + 1] = r[q].y; v[4 * q + 2] = r[q].z; v[4 * q + 3] = r[q].w;
-    }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
   }
 };
 
-size_t gate_vec_smem_bytes() { return sizeof(float) * 2 * kVKC * (kXT + kTE); }
-
-// logits[T, E] = x[T, d] . Wg[d, E] for larger batches: 256 threads on a 64-token x 64-expert
-// tile, 4 tokens x 4 experts per thread.  A warp spans 8 token groups x 4 expert groups, so
-// each step i reads 128 bytes of tokens and 64 bytes of gate weights per warp (two
-// shared-memory wavefronts for 16 multiply-adds per thread) and the kernel stays bound by
-// the FP32 pipe.  The token tile is stored i-major and widened to fp32; 64-wide chunks are
-// fetched into registers one chunk ahead.  Needs d % 16 == 0 and E % 4 == 0.
+// logits[T, E] = x[T, d] . Wg[d, E]; 256 threads, 4 x 4 outputs per thread.  The next chunk
+// is fetched into registers while the current one is multiplied (double-buffered tiles).
+// Vector path: d % 8 == 0 and E % 4 == 0 (16-byte loads); otherwise the scalar kernel below.
 template <typename Tin>
 __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict__ x,
                                                           const float* __restrict__ Wg, int T,
                                                           int d, int E,
                                                           float* __restrict__ logits) {
-  extern __shared__ __align__(16) float gsm[];
-  float (*xs)[kVKC][kXT] = reinterpret_cast<float (*)[kVKC][kXT]>(gsm);                 // [2]
-  float (*ws)[kVKC][kTE] = reinterpret_cast<float (*)[kVKC][kTE]>(gsm + 2 * kVKC * kXT);  // [2]
-  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
-  const int tg = (wp & 1) * 8 + (lane & 7);        // token group: tokens 4 tg .. 4 tg + 3
-  const int eg = (wp >> 1) * 4 + (lane >> 3);      // expert group: experts 4 eg .. 4 eg + 3
+  __shared__ __align__(16) float xs[2][kTT][kXP];   // token tile: xs[t][i]
+  __shared__ __align__(16) float ws[2][kKC][kTE];   // Wg tile: ws[i][e]
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
-  // loader roles: token row lt, columns lk .. lk+15; Wg rows lw + 16 r, experts le .. le+3
-  const int lt = threadIdx.x >> 2, lk = (threadIdx.x & 3) * 16;
+  // loader roles: token row lt, columns lk .. lk+7; Wg rows lw, lw+16 (4 experts at le)
+  const int lt = threadIdx.x >> 2, lk = (threadIdx.x & 3) * 8;
   const int lw = threadIdx.x >> 4, le = (threadIdx.x & 15) * 4;
   float acc[4][4];
 #pragma unroll
@@ -88,53 +69,47 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
 
   XChunk<Tin> xr;
-  float4 wr[4];
+  float4 wr0, wr1;
   auto fetch = [&](int k0) {
     const int t = t0 + lt;
-    const int kc = min(kVKC, d - k0);
+    const int kc = min(kKC, d - k0);
     if (t < T && lk < kc) xr.load(x + (size_t)t * d + k0 + lk);
     else xr.zero();
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     const bool eok = e0 + le < E;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int row = lw + 16 * r;
-      wr[r] = (eok && row < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + row) * E + e0 + le)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    wr0 = (eok && lw < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw) * E + e0 + le) : z;
+    wr1 = (eok && lw + 16 < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw + 16) * E + e0 + le) : z;
   };
   auto stash = [&](int buf) {
-    float v[16];
+    float v[8];
     xr.to_f32(v);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) xs[buf][lk + j][lt] = v[j];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) *reinterpret_cast<float4*>(&ws[buf][lw + 16 * r][le]) = wr[r];
+    *reinterpret_cast<float4*>(&xs[buf][lt][lk]) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(&xs[buf][lt][lk + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+    *reinterpret_cast<float4*>(&ws[buf][lw][le]) = wr0;
+    *reinterpret_cast<float4*>(&ws[buf][lw + 16][le]) = wr1;
   };
 
   fetch(0);
   stash(0);
   __syncthreads();
   int buf = 0;
-  for (int k0 = 0; k0 < d; k0 += kVKC) {
-    const int kc = min(kVKC, d - k0);
-    const bool more = k0 + kVKC < d;
-    if (more) fetch(k0 + kVKC);
-    // keep the prefetch loads above the multiply-adds: without this fence the compiler may
-    // sink them to their first use after the loop and serialise their latency with the math
-    asm volatile("" ::: "memory");
+  for (int k0 = 0; k0 < d; k0 += kKC) {
+    const int kc = min(kKC, d - k0);
+    const bool more = k0 + kKC < d;
+    if (more) fetch(k0 + kKC);
     auto step = [&](int kk) {                      // one i: 16 chained multiply-adds
-      const float4 a = *reinterpret_cast<const float4*>(&xs[buf][kk][tg * 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][eg * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float4 b = *reinterpret_cast<const float4*>(&ws[buf][kk][tx * 4]);
+      const float av[4] = {xs[buf][ty * 4][kk], xs[buf][ty * 4 + 1][kk], xs[buf][ty * 4 + 2][kk],
+                           xs[buf][ty * 4 + 3][kk]};
       const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
     };
-    if (kc == kVKC) {                              // full chunk: straight-line code
+    if (kc == kKC) {                               // full chunk: straight-line code
 #pragma unroll
-      for (int kk = 0; kk < kVKC; ++kk) step(kk);  // ascending i
+      for (int kk = 0; kk < kKC; ++kk) step(kk);   // ascending i
     } else {
       for (int kk = 0; kk < kc; ++kk) step(kk);    // ascending i, no padding steps
     }
@@ -144,9 +119,9 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int t = t0 + tg * 4 + i;
+    const int t = t0 + ty * 4 + i;
     if (t >= T) continue;
-    const int e = e0 + eg * 4;
+    const int e = e0 + tx * 4;
     if (e + 3 < E) {
       *reinterpret_cast<float4*>(logits + (size_t)t * E + e) =
           make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
@@ -295,101 +270,6 @@ __global__ void __launch_bounds__(256) gate_logits_small_kernel(const Tin* __res
   if (t < T && e < E) logits[(size_t)t * E + e] = acc;
 }
 
-// ---------------------------------------------------------------------------------------
-// Larger batches (f16 tokens): lane = token, 16 experts per thread.  Block = 8 warps over
-// 32 tokens x 128 experts.  Each step i reads the 16 gate weights of a warp's experts with
-// four warp-uniform (broadcast) 16-byte shared loads and takes the lane's token value from
-// registers, so one shared-memory wavefront feeds four multiply-add instructions.  Raw token
-// and Wg chunks stream through a three-deep cp.async ring.  Needs f16 tokens, d % 64 == 0,
-// E % 16 == 0, 16-byte aligned rows.
-constexpr int kLTok = 32;        // tokens per block (one per lane)
-constexpr int kLExp = 128;       // experts per block (16 per warp)
-constexpr int kLKC = 64;         // shared-dimension chunk
-constexpr int kLStages = 3;      // ring depth
-constexpr int kLXRow = kLKC + 8; // padded row (halves) of the raw token chunk
-
-__host__ __device__ constexpr size_t lane_slot_bytes() {
-  return (size_t)kLKC * kLExp * sizeof(float) + (size_t)kLTok * kLXRow * sizeof(__half);
-}
-
-__global__ void __launch_bounds__(256) gate_logits_lane_kernel(const __half* __restrict__ x,
-                                                               const float* __restrict__ Wg,
-                                                               int T, int d, int E,
-                                                               float* __restrict__ logits) {
-  extern __shared__ __align__(16) uint8_t lsm[];
-  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
-  const int t0 = blockIdx.x * kLTok, e0 = blockIdx.y * kLExp;
-  const int nch = d / kLKC;
-  constexpr size_t slot = lane_slot_bytes();
-  auto issue = [&](int c) {
-    uint8_t* base = lsm + (size_t)(c % kLStages) * slot;
-    const int k0 = c * kLKC;
-    // Wg rows k0 .. k0+63, experts e0 .. e0+127: 64 x 32 pieces of 16 bytes
-    for (int q = threadIdx.x; q < kLKC * (kLExp / 4); q += 256) {
-      const int row = q >> 5, col = (q & 31) * 4;
-      const int e = e0 + col;
-      cp_async16(base + ((size_t)row * kLExp + col) * 4, Wg + (size_t)(k0 + row) * E + min(e, E - 4),
-                 e < E ? 16 : 0);
-    }
-    // tokens t0 .. t0+31, columns k0 .. k0+63: 32 x 8 pieces
-    __half* xb = reinterpret_cast<__half*>(base + (size_t)kLKC * kLExp * 4);
-    {
-      const int q = threadIdx.x;                 // 256 pieces, one each
-      const int tt = q >> 3, col = (q & 7) * 8;
-      const int t = t0 + tt;
-      cp_async16(xb + tt * kLXRow + col, x + (size_t)min(t, T - 1) * d + k0 + col, t < T ? 16 : 0);
-    }
-  };
-#pragma unroll
-  for (int c = 0; c < kLStages - 1; ++c) {
-    if (c < nch) issue(c);
-    cp_async_commit();
-  }
-  float acc[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-  for (int c = 0; c < nch; ++c) {
-    if (c + kLStages - 1 < nch) issue(c + kLStages - 1);
-    cp_async_commit();
-    cp_async_wait<kLStages - 1>();
-    __syncthreads();
-    const uint8_t* base = lsm + (size_t)(c % kLStages) * slot;
-    const float* ws = reinterpret_cast<const float*>(base) + wp * 16;
-    const __half* xrow = reinterpret_cast<const __half*>(base + (size_t)kLKC * kLExp * 4) + lane * kLXRow;
-    __half2 xv[kLKC / 2];
-#pragma unroll
-    for (int q = 0; q < kLKC / 8; ++q) {
-      const uint4 u = *reinterpret_cast<const uint4*>(xrow + 8 * q);
-      const __half2* h = reinterpret_cast<const __half2*>(&u);
-      xv[4 * q] = h[0]; xv[4 * q + 1] = h[1]; xv[4 * q + 2] = h[2]; xv[4 * q + 3] = h[3];
-    }
-#pragma unroll
-    for (int kk = 0; kk < kLKC; ++kk) {           // ascending i
-      const float xi = (kk & 1) ? __high2float(xv[kk >> 1]) : __low2float(xv[kk >> 1]);
-      const float4* wr = reinterpret_cast<const float4*>(ws + (size_t)kk * kLExp);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 w4 = wr[q];                  // same address in every lane: a broadcast
-        acc[4 * q] = __fmaf_rn(xi, w4.x, acc[4 * q]);
-        acc[4 * q + 1] = __fmaf_rn(xi, w4.y, acc[4 * q + 1]);
-        acc[4 * q + 2] = __fmaf_rn(xi, w4.z, acc[4 * q + 2]);
-        acc[4 * q + 3] = __fmaf_rn(xi, w4.w, acc[4 * q + 3]);
-      }
-    }
-    __syncthreads();                               // the slot may be refilled next
-  }
-  cp_async_wait<0>();
-  const int t = t0 + lane;
-  if (t < T) {
-    const int e = e0 + wp * 16;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (e + 4 * q + 3 < E)
-        *reinterpret_cast<float4*>(logits + (size_t)t * E + e + 4 * q) =
-            make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-  }
-}
-
 // (v, i) beats (w, j) when v > w, or v == w and i < j: descending logit, ties to lower index.
 __device__ __forceinline__ bool beats(float v, int i, float w, int j) {
   return v > w || (v == w && i < j);
@@ -474,37 +354,18 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
     }
     return cudaGetLastError();
   }
-  if (dtype_f16 && d % kLKC == 0 && E % 16 == 0 && aligned) {
-    cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(gate_logits_lane_kernel));
-    if (err != cudaSuccess) return err;
-    dim3 g((T + kLTok - 1) / kLTok, (E + kLExp - 1) / kLExp);
-    gate_logits_lane_kernel<<<g, 256, kLStages * lane_slot_bytes(), s>>>(
-        static_cast<const __half*>(x), Wg, T, d, E, logits);
-    return cudaGetLastError();
-  }
   dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);
-  const bool vec = d % 16 == 0 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+  const bool vec = d % 8 == 0 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(Wg) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
-  const size_t vsmem = gate_vec_smem_bytes();
   if (dtype_f16) {
     const __half* xh = static_cast<const __half*>(x);
-    if (vec) {
-      cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(gate_logits_kernel<__half>));
-      if (err != cudaSuccess) return err;
-      gate_logits_kernel<__half><<<grid, 256, vsmem, s>>>(xh, Wg, T, d, E, logits);
-    } else {
-      gate_logits_scalar_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
-    }
+    if (vec) gate_logits_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
+    else gate_logits_scalar_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
   } else {
     const float* xf = static_cast<const float*>(x);
-    if (vec) {
-      cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(gate_logits_kernel<float>));
-      if (err != cudaSuccess) return err;
-      gate_logits_kernel<float><<<grid, 256, vsmem, s>>>(xf, Wg, T, d, E, logits);
-    } else {
-      gate_logits_scalar_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
-    }
+    if (vec) gate_logits_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
+    else gate_logits_scalar_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
   }
   return cudaGetLastError();
 }
