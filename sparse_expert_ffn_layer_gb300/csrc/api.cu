@@ -261,6 +261,11 @@ void fill_common(GemmArgs& g, const TcPlan& p, int E, int mw, int* status) {
 thread_local cudaEvent_t* t_stage_events = nullptr;
 thread_local cudaEvent_t t_stage_store[MOE_STAGE_EVENTS];
 
+// Kernels after the first of a call are launched with programmatic dependent launch: each
+// starts its prologue while its predecessor drains.  Not while stage events are recorded, so
+// that every stage boundary is a full one.
+bool use_pdl() { return t_stage_events == nullptr; }
+
 // Inside a stream capture the events are recorded as external event nodes, so that each
 // replay of the graph records them (a plain record would only order the capture).
 cudaError_t stage_mark(int i, cudaStream_t s) {
@@ -285,8 +290,9 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
                       int d, int f, int E, int f_res, int S_rows, int rows_bound, __half* H,
                       __half* Hres, int mode, void* out, float* acc32, float* r32,
                       const float* slot_w, const int32_t* drop_slot_of, float* partial,
-                      size_t partial_bytes, int* status, cudaStream_t s) {
+                      size_t partial_bytes, int* status, bool pdl_first, cudaStream_t s) {
   const bool residual = Wr1 != nullptr;
+  const bool pdl = use_pdl();
   // first GEMM: tiles of at most 64 token rows, so that items can span four weight blocks and
   // each gathered row (a tile::gather4 TMA instruction per four rows) feeds four MMAs
   TcPlan plan1, plan2;
@@ -354,8 +360,8 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   g1.part_rows = part_rows;
   g1.part_cols = std::max(f, residual ? f_res : 0);
   g1.part_res_row0 = S_rows;
-  MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan1.grid, s));
-  if (ks1 > 1) MOE_TRY(launch_splitk_reduce1(g1, S_rows, T_res, f, f_res, s));
+  MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan1.grid, s, pdl && pdl_first));
+  if (ks1 > 1) MOE_TRY(launch_splitk_reduce1(g1, S_rows, T_res, f, f_res, s, pdl));
   MOE_TRY(stage_mark(4, s));
 
   GemmArgs g2;
@@ -380,8 +386,8 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   g2.part_rows = part_rows;
   g2.part_cols = d;
   g2.part_res_row0 = S_rows;
-  MOE_TRY(launch_grouped_gemm2(mW2, mH, mWr2, mHres, g2, plan2.grid, s));
-  if (ks2 > 1) MOE_TRY(launch_splitk_reduce2(g2, S_rows, T_res, d, s));
+  MOE_TRY(launch_grouped_gemm2(mW2, mH, mWr2, mHres, g2, plan2.grid, s, pdl));
+  if (ks2 > 1) MOE_TRY(launch_splitk_reduce2(g2, S_rows, T_res, d, s, pdl));
   MOE_TRY(stage_mark(5, s));
   return MOE_OK;
 }
@@ -429,7 +435,7 @@ moe_status expert_ffn_on_scratch(const void* tokens, const int32_t* perm, const 
   if (dtype == MOE_F16) {
     return run_tc_ffn(tokens, perm, offsets, W1, W2, nullptr, nullptr, T, d, f, E, 0, S_max, S_max,
                       reinterpret_cast<__half*>(scratch), nullptr, kModeExpertOut, expert_out,
-                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, s);
+                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, /*pdl_first=*/false, s);
   }
   SimtArgs a;
   memset(&a, 0, sizeof(a));
@@ -486,7 +492,8 @@ moe_status moe_gate_topk(const void* tokens, moe_dtype dtype, const float* Wg,
   } else {
     if (!logits_out) return MOE_ERR_INVALID_ARG;   // the logits need a home
     MOE_TRY(launch_gate_logits(tokens, dtype == MOE_F16, Wg, T, d, E, logits_out, s));
-    MOE_TRY(launch_softmax_topk(logits_out, T, E, k, probs_out, topk_idx, topk_w, nullptr, s));
+    MOE_TRY(launch_softmax_topk(logits_out, T, E, k, probs_out, topk_idx, topk_w, nullptr, s,
+                                use_pdl()));
   }
   return MOE_OK;
 }
@@ -526,7 +533,7 @@ moe_status moe_expert_ffn(const void* tokens, const int32_t* perm, const int32_t
   if (f16) {
     return run_tc_ffn(tokens, perm, offsets, W1, W2, nullptr, nullptr, T, d, f, E, 0, S_max, S_max,
                       reinterpret_cast<__half*>(ws + kAlign), nullptr, kModeExpertOut, expert_out,
-                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, s);
+                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, /*pdl_first=*/false, s);
   }
   SimtArgs a;
   memset(&a, 0, sizeof(a));
@@ -602,10 +609,10 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
   MOE_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
   MOE_TRY(launch_gate_logits(tokens, f16, Wg, T, d, E, logits, s));
   MOE_TRY(stage_mark(1, s));
-  MOE_TRY(launch_softmax_topk(logits, T, E, k, nullptr, topk_idx, topk_w, nullptr, s));
+  MOE_TRY(launch_softmax_topk(logits, T, E, k, nullptr, topk_idx, topk_w, nullptr, s, use_pdl()));
   MOE_TRY(stage_mark(2, s));
   MOE_TRY(launch_dispatch(topk_idx, T, k, E, C, counts, kept, offsets, perm, slot_of, topk_w, slot_w,
-                          s));
+                          s, use_pdl()));
   MOE_TRY(stage_mark(3, s));
   const int rows_bound = std::max(std::min(C, T * k), residual ? T : 0);
   if (f16) {
@@ -615,7 +622,7 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
                     residual ? reinterpret_cast<__half*>(ws + L.Hres) : nullptr, mode, out, acc32, r32,
                     slot_w, k == 1 ? slot_of : nullptr,
                     L.partial_bytes ? reinterpret_cast<float*>(ws + L.partial) : nullptr,
-                    L.partial_bytes, status, s);
+                    L.partial_bytes, status, /*pdl_first=*/true, s);
     if (st != MOE_OK) return st;
   } else {
     SimtArgs a;
@@ -642,7 +649,7 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
     MOE_TRY(launch_simt_ffn2(a, rows_bound, s));
     MOE_TRY(stage_mark(5, s));
   }
-  if (mode == kModeAccum) MOE_TRY(launch_finalize(acc32, r32, T, d, f16, out, s));
+  if (mode == kModeAccum) MOE_TRY(launch_finalize(acc32, r32, T, d, f16, out, s, f16 && use_pdl()));
   MOE_TRY(stage_mark(6, s));
   return MOE_OK;
 }

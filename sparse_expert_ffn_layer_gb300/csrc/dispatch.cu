@@ -57,6 +57,8 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
   const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int q = threadIdx.x; q < kWarps * E; q += blockDim.x) cnt[q] = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
 
   const int L = (n + kWarps - 1) / kWarps;
@@ -229,7 +231,7 @@ constexpr size_t kDispatchSmemMax = 200 * 1024;
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C, int32_t* counts_raw,
                             int32_t* kept, int32_t* offsets, int32_t* perm, int32_t* slot_of,
-                            const float* topk_w, float* slot_w, cudaStream_t s) {
+                            const float* topk_w, float* slot_w, cudaStream_t s, bool pdl) {
   const int n = T * k;
   const int S_cap = (int)std::min<long long>(n, (long long)E * C);
   size_t smem = dispatch_smem_bytes(E);
@@ -240,9 +242,8 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C,
   auto kern = in_regs ? dispatch_kernel<kRegBatches> : dispatch_kernel<0>;
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern));
   if (err != cudaSuccess) return err;
-  kern<<<1, kWarps * 32, smem, s>>>(topk_idx, n, k, E, C, counts_raw, kept, offsets,
-                                    perm, slot_of, topk_w, slot_w, S_cap, stage_out);
-  return cudaGetLastError();
+  return launch_k(kern, 1, kWarps * 32, smem, s, pdl, topk_idx, n, k, E, C, counts_raw, kept,
+                  offsets, perm, slot_of, topk_w, slot_w, S_cap, stage_out);
 }
 
 }  // namespace moe

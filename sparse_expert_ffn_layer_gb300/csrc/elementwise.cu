@@ -62,6 +62,8 @@ __device__ __forceinline__ float as_f32<__half>(__half v) { return __half2float(
 template <typename Tout>
 __global__ void finalize_kernel(const float* __restrict__ acc32, const float* __restrict__ r32,
                                 size_t n, Tout* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n / 4; i += stride) {
     float4 v = reinterpret_cast<const float4*>(acc32)[i];
@@ -118,6 +120,8 @@ __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
 
 // Split-K reduction of the first GEMM: sum the chunks in order, GeLU, round to f16.
 __global__ void splitk_reduce1_kernel(const GemmArgs g, int S_max, int T_res, int f, int f_res) {
+  pdl_wait();
+  pdl_trigger();
   const int S = g.offsets[g.E];
   const size_t n = (size_t)(S_max + T_res) * g.part_cols;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -136,6 +140,8 @@ __global__ void splitk_reduce1_kernel(const GemmArgs g, int S_max, int T_res, in
 
 // Split-K reduction of the second GEMM: sum the chunks in order, then the combine.
 __global__ void splitk_reduce2_kernel(const GemmArgs g, int S_max, int T_res, int d) {
+  pdl_wait();
+  pdl_trigger();
   const int S = g.offsets[g.E];
   const size_t n = (size_t)(S_max + T_res) * d;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -162,16 +168,16 @@ __global__ void splitk_reduce2_kernel(const GemmArgs g, int S_max, int T_res, in
 }  // namespace
 
 cudaError_t launch_splitk_reduce1(const GemmArgs& g, int S_max, int T_res, int f, int f_res,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, bool pdl) {
   const size_t n = (size_t)(S_max + T_res) * g.part_cols;
-  splitk_reduce1_kernel<<<grid_for(n, 256), 256, 0, s>>>(g, S_max, T_res, f, f_res);
-  return cudaGetLastError();
+  return launch_k(splitk_reduce1_kernel, grid_for(n, 256), 256, 0, s, pdl, g, S_max, T_res, f,
+                  f_res);
 }
 
-cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d, cudaStream_t s) {
+cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d, cudaStream_t s,
+                                  bool pdl) {
   const size_t n = (size_t)(S_max + T_res) * d;
-  splitk_reduce2_kernel<<<grid_for(n, 256), 256, 0, s>>>(g, S_max, T_res, d);
-  return cudaGetLastError();
+  return launch_k(splitk_reduce2_kernel, grid_for(n, 256), 256, 0, s, pdl, g, S_max, T_res, d);
 }
 
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s) {
@@ -188,12 +194,13 @@ cudaError_t launch_zero_dropped_rows(const int32_t* slot_of, int T, int k, int d
 }
 
 cudaError_t launch_finalize(const float* acc32, const float* r32, int T, int d, int dtype_f16,
-                            void* out, cudaStream_t s) {
+                            void* out, cudaStream_t s, bool pdl) {
   const size_t n = (size_t)T * d;
   const int g = grid_for(n / 4, 256);
-  if (dtype_f16) finalize_kernel<__half><<<g, 256, 0, s>>>(acc32, r32, n, static_cast<__half*>(out));
-  else finalize_kernel<float><<<g, 256, 0, s>>>(acc32, r32, n, static_cast<float*>(out));
-  return cudaGetLastError();
+  if (dtype_f16)
+    return launch_k(finalize_kernel<__half>, g, 256, 0, s, pdl, acc32, r32, n,
+                    static_cast<__half*>(out));
+  return launch_k(finalize_kernel<float>, g, 256, 0, s, pdl, acc32, r32, n, static_cast<float*>(out));
 }
 
 cudaError_t launch_combine(const void* expert_out, const int32_t* slot_of, const float* topk_w,

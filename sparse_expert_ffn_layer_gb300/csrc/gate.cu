@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
                                                           const float* __restrict__ Wg, int T,
                                                           int d, int E,
                                                           float* __restrict__ logits) {
+  pdl_trigger();   // the top-k kernel may start its launch; it waits for these logits
   __shared__ __align__(16) float xs[2][kTT][kXP];   // token tile: xs[t][i]
   __shared__ __align__(16) float ws[2][kKC][kTE];   // Wg tile: ws[i][e]
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(256) gate_logits_scalar_kernel(const Tin* __re
                                                                  const float* __restrict__ Wg,
                                                                  int T, int d, int E,
                                                                  float* __restrict__ logits) {
+  pdl_trigger();   // the top-k kernel may start its launch; it waits for these logits
   __shared__ float xs[kTT][kKC + 1];
   __shared__ __align__(16) float ws[kKC][kTE];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(256) gate_logits_small_kernel(const Tin* __res
                                                                 const float* __restrict__ Wg,
                                                                 int T, int d, int E,
                                                                 float* __restrict__ logits) {
+  pdl_trigger();   // the top-k kernel may start its launch; it waits for these logits
   extern __shared__ __align__(16) uint8_t ssm[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int e0 = blockIdx.x * kSExp, t0 = blockIdx.y * kSTok;
@@ -291,6 +294,8 @@ __global__ void __launch_bounds__(256) softmax_topk_kernel(const float* __restri
                                                            int32_t* __restrict__ topk_idx,
                                                            float* __restrict__ topk_w,
                                                            float* __restrict__ logits_copy) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -372,12 +377,10 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
 
 cudaError_t launch_softmax_topk(const float* logits, int T, int E, int k, float* probs_out,
                                 int32_t* topk_idx, float* topk_w, float* logits_copy,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool pdl) {
   const int warps = 8;
-  softmax_topk_kernel<<<(T + warps - 1) / warps, warps * 32, 0, s>>>(logits, T, E, k, probs_out,
-                                                                      topk_idx, topk_w,
-                                                                      logits_copy);
-  return cudaGetLastError();
+  return launch_k(softmax_topk_kernel, (T + warps - 1) / warps, warps * 32, 0, s, pdl, logits, T, E,
+                  k, probs_out, topk_idx, topk_w, logits_copy);
 }
 
 }  // namespace moe

@@ -23,6 +23,8 @@
 // slot order plus, for the residual variant, one group of all T tokens using the dense MLP
 // weights (PR-MoE's fixed MLP, DeepSpeed-MoE review "Phenomenon2": Residual-MoE).
 // Every wait is bounded: a stalled pipeline records MOE_ERR_TIMEOUT and the CTA leaves.
+#include <algorithm>
+
 #include "launch.h"
 
 namespace moe {
@@ -142,6 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) tmem_alloc(tmem_holder, a.tmem_cols);
+  // everything above is independent of the previous kernel of the stream; from here on its
+  // results (offsets, gathered rows, H) are read and its inputs may be overwritten
+  pdl_wait();
+  pdl_trigger();
   // chunk prefix over experts (warp 2), E <= 1024
   if (warp == 2) {
     for (int e = lane; e <= a.E; e += 32) soffs[e] = a.offsets[e];
@@ -408,23 +414,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, a.tmem_cols);
 }
 
+// Dynamic shared memory of a launch is at least this much, so that no two CTAs of these
+// kernels are ever resident on one SM (an SM has 228 KB): a CTA that starts early under
+// programmatic dependent launch can then never wait in tcgen05.alloc for columns held by a
+// CTA of the previous GEMM on the same SM.
+constexpr size_t kMinGemmSmem = 116 * 1024;
+
 template <bool G, int Epi, int MW>
 cudaError_t launch_mw(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
-                      const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s) {
+                      const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s,
+                      bool pdl) {
   const SmemLayout L = smem_layout(args.nmax, args.stages, args.E, MW);
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_kernel<G, Epi, MW>));
   if (err != cudaSuccess) return err;
-  grouped_gemm_kernel<G, Epi, MW><<<grid, kThreads, L.total, s>>>(A, B, Ar, Br, args);
-  return cudaGetLastError();
+  return launch_k(grouped_gemm_kernel<G, Epi, MW>, grid, kThreads,
+                  std::max<size_t>(L.total, kMinGemmSmem), s, pdl, A, B, Ar, Br, args);
 }
 
 template <bool G, int Epi>
 cudaError_t launch_one(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
-                       const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s) {
+                       const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s,
+                       bool pdl) {
   switch (args.mw) {
-    case 1: return launch_mw<G, Epi, 1>(A, B, Ar, Br, args, grid, s);
-    case 2: return launch_mw<G, Epi, 2>(A, B, Ar, Br, args, grid, s);
-    case 4: return launch_mw<G, Epi, 4>(A, B, Ar, Br, args, grid, s);
+    case 1: return launch_mw<G, Epi, 1>(A, B, Ar, Br, args, grid, s, pdl);
+    case 2: return launch_mw<G, Epi, 2>(A, B, Ar, Br, args, grid, s, pdl);
+    case 4: return launch_mw<G, Epi, 4>(A, B, Ar, Br, args, grid, s, pdl);
   }
   return cudaErrorInvalidValue;
 }
@@ -439,14 +453,14 @@ int gemm_stages_for(int nmax, int E, int mw, int smem_limit) {
 
 cudaError_t launch_grouped_gemm1(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                                  const CUtensorMap& Br, const GemmArgs& args, int grid,
-                                 cudaStream_t s) {
-  return launch_one<true, kEpiGeluH>(A, B, Ar, Br, args, grid, s);
+                                 cudaStream_t s, bool pdl) {
+  return launch_one<true, kEpiGeluH>(A, B, Ar, Br, args, grid, s, pdl);
 }
 
 cudaError_t launch_grouped_gemm2(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                                  const CUtensorMap& Br, const GemmArgs& args, int grid,
-                                 cudaStream_t s) {
-  return launch_one<false, kEpiCombine>(A, B, Ar, Br, args, grid, s);
+                                 cudaStream_t s, bool pdl) {
+  return launch_one<false, kEpiCombine>(A, B, Ar, Br, args, grid, s, pdl);
 }
 
 }  // namespace moe

@@ -1,9 +1,30 @@
 // Internal interface between the C-ABI front end (api.cu) and the kernels.
 #pragma once
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace moe {
+
+// Launches `kernel`; with pdl the launch carries programmatic stream serialisation, so the
+// grid may start while the previous kernel of the stream finishes (the kernel itself waits
+// with pdl_wait() before touching that kernel's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Epilogue kinds of the grouped GEMM.
 enum : int { kEpiGeluH = 0, kEpiCombine = 1 };
@@ -66,11 +87,12 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
                                float* logits, cudaStream_t s);
 cudaError_t launch_softmax_topk(const float* logits, int T, int E, int k, float* probs_out,
                                 int32_t* topk_idx, float* topk_w, float* logits_copy,
-                                cudaStream_t s);
+                                cudaStream_t s, bool pdl = false);
 size_t dispatch_smem_bytes(int E);
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C,
                             int32_t* counts_raw, int32_t* kept, int32_t* offsets, int32_t* perm,
-                            int32_t* slot_of, const float* topk_w, float* slot_w, cudaStream_t s);
+                            int32_t* slot_of, const float* topk_w, float* slot_w, cudaStream_t s,
+                            bool pdl = false);
 
 int gemm_stages_for(int nmax, int E, int mw, int smem_limit);
 // Raises the kernel's dynamic shared-memory limit to the device maximum, once per kernel
@@ -78,10 +100,10 @@ int gemm_stages_for(int nmax, int E, int mw, int smem_limit);
 cudaError_t ensure_smem_attr(const void* kernel);
 cudaError_t launch_grouped_gemm1(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                                  const CUtensorMap& Br, const GemmArgs& args, int grid,
-                                 cudaStream_t s);
+                                 cudaStream_t s, bool pdl = false);
 cudaError_t launch_grouped_gemm2(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                                  const CUtensorMap& Br, const GemmArgs& args, int grid,
-                                 cudaStream_t s);
+                                 cudaStream_t s, bool pdl = false);
 
 // fp32 SIMT path (small layers)
 struct SimtArgs {
@@ -109,7 +131,7 @@ cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
 cudaError_t launch_zero_dropped_rows(const int32_t* slot_of, int T, int k, int d, int dtype_f16,
                                      void* out, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc32, const float* r32, int T, int d, int dtype_f16,
-                            void* out, cudaStream_t s);
+                            void* out, cudaStream_t s, bool pdl = false);
 cudaError_t launch_combine(const void* expert_out, const int32_t* slot_of, const float* topk_w,
                            const void* residual_in, int dtype_f16, int T, int d, int k, void* out,
                            cudaStream_t s);
@@ -117,7 +139,8 @@ cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t 
 // split-K reductions (fixed chunk order): first GEMM -> GeLU -> H / Hres; second GEMM -> the
 // combine of the given mode / r32
 cudaError_t launch_splitk_reduce1(const GemmArgs& g, int S_max, int T_res, int f, int f_res,
-                                  cudaStream_t s);
-cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d, cudaStream_t s);
+                                  cudaStream_t s, bool pdl = false);
+cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d, cudaStream_t s,
+                                  bool pdl = false);
 
 }  // namespace moe
