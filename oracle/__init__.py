@@ -49,6 +49,8 @@ def lib():
         L.oracle_capacity.restype = _I
         L.oracle_dispatch.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]
         L.oracle_dispatch.restype = _I
+        L.oracle_dispatch_shard.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+        L.oracle_dispatch_shard.restype = _I
         L.oracle_gelu.argtypes = [ctypes.c_double]
         L.oracle_gelu.restype = ctypes.c_double
         L.oracle_expert_ffn.argtypes = [_P, _I, _P, _P, _I, _I, _I, _P]
@@ -136,6 +138,31 @@ def dispatch(topk_idx: np.ndarray, E: int, C: int) -> Dispatch:
     slot_of = np.empty((T, k), np.int32)
     S = lib().oracle_dispatch(idx.ctypes.data, T, E, k, C, counts.ctypes.data, kept.ctypes.data,
                               offs.ctypes.data, perm.ctypes.data, slot_of.ctypes.data)
+    return Dispatch(C, counts, kept, offs, perm[:S].copy(), slot_of)
+
+
+def shard_bases(counts_per_shard: np.ndarray) -> np.ndarray:
+    """base[r, e] = assignments to expert e in shards 0 .. r-1 (shards in token order)."""
+    counts = np.asarray(counts_per_shard, np.int64)
+    base = np.zeros_like(counts)
+    for r in range(1, counts.shape[0]):
+        base[r] = base[r - 1] + counts[r - 1]
+    return base.astype(np.int32)
+
+
+def dispatch_shard(topk_idx: np.ndarray, E: int, C: int, base: np.ndarray) -> Dispatch:
+    """Dispatch of one shard of a token-sharded batch; C is the whole batch's capacity."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    b = _c(base, np.int32)
+    counts = np.empty(E, np.int32)
+    kept = np.empty(E, np.int32)
+    offs = np.empty(E + 1, np.int32)
+    perm = np.full(max(1, T * k), -1, np.int32)
+    slot_of = np.empty((T, k), np.int32)
+    S = lib().oracle_dispatch_shard(idx.ctypes.data, T, E, k, C, b.ctypes.data, counts.ctypes.data,
+                                    kept.ctypes.data, offs.ctypes.data, perm.ctypes.data,
+                                    slot_of.ctypes.data)
     return Dispatch(C, counts, kept, offs, perm[:S].copy(), slot_of)
 
 

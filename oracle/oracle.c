@@ -169,6 +169,51 @@ int oracle_dispatch(const int32_t* topk_idx, int T, int E, int k, int C, int32_t
   return offsets[E];
 }
 
+/*
+ * Step 3b for one shard of a batch that is split over ranks in token order
+ * (shard r holds a contiguous run of tokens, after those of shards 0 .. r-1).
+ * base[e] = assignments to expert e in the earlier shards.  The assignment's
+ * rank in the whole batch is base[e] + its rank within the shard, and the
+ * capacity rule of step 3b applies to that rank, with C the whole batch's
+ * capacity.  Outputs are those of oracle_dispatch for the shard's own tokens:
+ * counts_raw / kept of this shard, compact slots over its kept assignments,
+ * perm holding shard-local token indices.  Experts outside [0, E) are not
+ * counted and their assignments are dropped.  Returns the shard's S.
+ */
+int oracle_dispatch_shard(const int32_t* topk_idx, int T, int E, int k, int C,
+                          const int32_t* base, int32_t* counts_raw, int32_t* kept,
+                          int32_t* offsets, int32_t* perm, int32_t* slot_of) {
+  int32_t* rank = (int32_t*)malloc(sizeof(int32_t) * ((size_t)T * k + 1));
+  for (int e = 0; e < E; ++e) counts_raw[e] = 0;
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      size_t a = (size_t)t * k + j;
+      int e = topk_idx[a];
+      rank[a] = (e >= 0 && e < E) ? counts_raw[e]++ : -1;
+    }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    long long left = (long long)C - base[e];            /* capacity left for this shard */
+    if (left < 0) left = 0;
+    kept[e] = counts_raw[e] < left ? counts_raw[e] : (int32_t)left;
+    offsets[e + 1] = offsets[e] + kept[e];
+  }
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      size_t a = (size_t)t * k + j;
+      int e = topk_idx[a];
+      if (rank[a] >= 0 && (long long)base[e] + rank[a] < C) {
+        int s = offsets[e] + rank[a];
+        slot_of[a] = s;
+        perm[s] = t;
+      } else {
+        slot_of[a] = -1;
+      }
+    }
+  free(rank);
+  return offsets[E];
+}
+
 double oracle_gelu(double x) {
   const double c = sqrt(2.0 / M_PI);
   return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));

@@ -220,6 +220,64 @@ def test_dispatch_invariants(oracle_mod):
                     assert dsp.offsets[idx[t, j]] <= s < dsp.offsets[idx[t, j] + 1]
 
 
+def _shard_cuts(rng, T, R):
+    """Token ranges of R shards in token order (some may be empty)."""
+    return np.concatenate([[0], np.sort(rng.integers(0, T + 1, R - 1)), [T]]).astype(int)
+
+
+def test_dispatch_shard_equals_whole_batch(oracle_mod):
+    """A batch split over ranks in token order: with each shard's bases = the earlier shards'
+    counts, the kept / dropped decisions and every expert's token order equal those of the
+    whole batch (pinned by the stable-sort brute force)."""
+    rng = np.random.default_rng(6)
+    for trial in range(300):
+        T = int(rng.integers(1, 40))
+        E = int(rng.integers(1, 6))
+        k = 1 if E == 1 else int(rng.integers(1, 3))
+        idx = np.array([rng.choice(E, k, replace=False) for _ in range(T)], np.int32).reshape(T, k)
+        if trial % 3 == 0:
+            idx[:, 0] = rng.integers(0, min(E, 2), T)       # skewed first choices
+            if k == 2:
+                idx[:, 1] = (idx[:, 0] + 1 + rng.integers(0, E - 1, T)) % E
+        cf = float(rng.choice([0.5, 1.0, 1.25, 2.0]))
+        C = oracle_mod.capacity(T, E, cf)
+        counts, kept, offs, perm, slot = _dispatch_bruteforce(idx, E, C)
+        R = int(rng.integers(1, 5))
+        cuts = _shard_cuts(rng, T, R)
+        per = np.array([np.bincount(idx[cuts[r]:cuts[r + 1]].reshape(-1), minlength=E)
+                        for r in range(R)])
+        bases = oracle_mod.shard_bases(per)
+        assert np.array_equal(bases[0], np.zeros(E))
+        kept_sum = np.zeros(E, np.int64)
+        for r in range(R):
+            lo, hi = cuts[r], cuts[r + 1]
+            got = oracle_mod.dispatch_shard(idx[lo:hi], E, C, bases[r])
+            assert np.array_equal(got.counts_raw, per[r])
+            kept_sum += got.kept
+            assert np.array_equal(got.slot_of >= 0, slot[lo:hi] >= 0)
+            for e in range(E):
+                mine = got.perm[got.offsets[e]:got.offsets[e + 1]] + lo
+                whole = perm[offs[e]:offs[e + 1]]
+                assert np.array_equal(mine, whole[(whole >= lo) & (whole < hi)])
+            for t in range(hi - lo):
+                for j in range(k):
+                    if got.slot_of[t, j] >= 0:
+                        assert got.perm[got.slot_of[t, j]] == t
+        assert np.array_equal(kept_sum, kept)
+
+
+def test_dispatch_single_shard_is_plain_dispatch(oracle_mod):
+    rng = np.random.default_rng(7)
+    for _ in range(50):
+        T, E = int(rng.integers(1, 50)), int(rng.integers(2, 9))
+        idx = np.array([rng.choice(E, 2, replace=False) for _ in range(T)], np.int32)
+        C = oracle_mod.capacity(T, E, float(rng.choice([0.5, 1.0, 1.25])))
+        a = oracle_mod.dispatch(idx, E, C)
+        b = oracle_mod.dispatch_shard(idx, E, C, np.zeros(E, np.int32))
+        for f in ("counts_raw", "kept", "offsets", "perm", "slot_of"):
+            assert np.array_equal(getattr(a, f), getattr(b, f)), f
+
+
 # ---------------------------------------------------------------- GeLU and the MLP
 def test_gelu_identities_and_library(oracle_mod):
     import torch
