@@ -124,6 +124,31 @@ MOE_API moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k, fl
                         int32_t* slot_of, moe_stream_t stream);
 
 /*
+ * Dispatch of one shard of a token-sharded batch, with the whole batch's capacity rule.
+ * The pages have no multi-GPU data-parallel layout of this layer (their own design is expert
+ * parallelism); this entry is the one exchange step that token sharding needs so that
+ * routing does not depend on how the batch is split (capacity as above: the DeepSpeed-MoE
+ * review, "Phenomenon2", read as ceil(cf T / E) in token order).
+ *   The batch of T_global tokens is split over n_ranks callers in token order; this call
+ *   holds shard `rank` (T tokens).  counts_all [n_ranks, E] int32 (device; nullable when
+ *   rank == 0): the counts_raw of every shard in rank order, exchanged by the caller (for
+ *   example an all_gather of each shard's counts_raw from moe_dispatch).
+ *   C = ceil(cf T_global / E).  An assignment is kept iff (assignments to its expert in
+ *   earlier shards) + (its rank within this shard) < C, so the kept / dropped decisions are
+ *   those of moe_dispatch on the whole batch.
+ *   Outputs as moe_dispatch, local to the shard: counts_raw / kept per expert for this
+ *   shard, offsets / perm / slot_of over this shard's compact slots (perm holds local token
+ *   indices), perm sized min(T k, E C).
+ * Errors: MOE_ERR_INVALID_ARG for T_global < T, rank outside [0, n_ranks), or counts_all
+ * NULL with rank > 0; otherwise as moe_dispatch.  T = 0 is a valid no-op.
+ */
+MOE_API moe_status moe_dispatch_sharded(const int32_t* topk_idx, int T, int E, int k,
+                                        float capacity_factor, int T_global,
+                                        const int32_t* counts_all, int n_ranks, int rank,
+                                        int32_t* counts_raw, int32_t* kept, int32_t* offsets,
+                                        int32_t* perm, int32_t* slot_of, moe_stream_t stream);
+
+/*
  * Grouped expert FFN over the dispatched slots, unscaled:
  *   expert_out[s, :] = GeLU_tanh(tokens[perm[s], :] W1[e]) W2[e]   for s in expert e's slots.
  *   tokens [T, d], W1 [E, d, f], W2 [E, f, d], expert_out [S_max, d]: all in `dtype`.

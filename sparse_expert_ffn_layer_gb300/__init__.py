@@ -22,7 +22,7 @@ MOE_MLP_STANDARD, MOE_MLP_RESIDUAL = 0, 1
 EXPORTED = ("moe_capacity", "moe_workspace_size", "moe_gate_topk", "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_status_read",
             "moe_status_string", "moe_selftest_wait", "moe_set_stage_events",
-            "moe_expert_ffn_noalloc")
+            "moe_expert_ffn_noalloc", "moe_dispatch_sharded")
 
 _lib = None
 MOE_STAGE_EVENTS = 7
@@ -53,6 +53,7 @@ def get_lib():
         "moe_selftest_wait": ([P, ctypes.c_uint64, P], I),
         "moe_set_stage_events": ([P, I], I),
         "moe_expert_ffn_noalloc": ([P, P, P, P, P, I, I, I, I, I, I, P, P], I),
+        "moe_dispatch_sharded": ([P, I, I, I, F, I, P, I, I, P, P, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -130,6 +131,16 @@ def moe_dispatch(topk_idx, E, capacity_factor, counts_raw, kept, offsets, perm, 
     _check(get_lib().moe_dispatch(_ptr(topk_idx), T, E, k, capacity_factor, _ptr(counts_raw), _ptr(kept),
                             _ptr(offsets), _ptr(perm), _ptr(slot_of), _stream(stream)),
            "moe_dispatch")
+
+
+def moe_dispatch_sharded(topk_idx, E, capacity_factor, T_global, counts_all, rank, counts_raw, kept,
+                         offsets, perm, slot_of, stream=None):
+    T, k = topk_idx.shape
+    n_ranks = counts_all.shape[0] if counts_all is not None else 1
+    _check(get_lib().moe_dispatch_sharded(_ptr(topk_idx), T, E, k, capacity_factor, T_global,
+                                          _ptr(counts_all), n_ranks, rank, _ptr(counts_raw),
+                                          _ptr(kept), _ptr(offsets), _ptr(perm), _ptr(slot_of),
+                                          _stream(stream)), "moe_dispatch_sharded")
 
 
 def moe_expert_ffn(tokens, perm, offsets, W1, W2, S_max, expert_out, workspace, stream=None):

@@ -512,6 +512,25 @@ moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k, float capa
   return MOE_OK;
 }
 
+moe_status moe_dispatch_sharded(const int32_t* topk_idx, int T, int E, int k,
+                                float capacity_factor, int T_global, const int32_t* counts_all,
+                                int n_ranks, int rank, int32_t* counts_raw, int32_t* kept,
+                                int32_t* offsets, int32_t* perm, int32_t* slot_of,
+                                moe_stream_t stream) {
+  if (T < 0 || T_global < T || E < 1 || (k != 1 && k != 2) || k > E) return MOE_ERR_INVALID_ARG;
+  if (n_ranks < 1 || rank < 0 || rank >= n_ranks) return MOE_ERR_INVALID_ARG;
+  const int C = capacity_of(T_global, E, capacity_factor);
+  if (C < 0) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || (long long)T_global * k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!topk_idx || !counts_raw || !kept || !offsets || !perm || !slot_of) return MOE_ERR_INVALID_ARG;
+  if (rank > 0 && !counts_all) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(launch_dispatch(topk_idx, T, k, E, C, counts_raw, kept, offsets, perm, slot_of, nullptr,
+                          nullptr, reinterpret_cast<cudaStream_t>(stream), false,
+                          rank > 0 ? counts_all : nullptr, rank));
+  return MOE_OK;
+}
+
 moe_status moe_expert_ffn(const void* tokens, const int32_t* perm, const int32_t* offsets,
                           const void* W1, const void* W2, moe_dtype dtype, int T, int d, int f,
                           int E, int S_max, void* expert_out, void* workspace, size_t ws_bytes,

@@ -16,6 +16,12 @@
 // Pass 3: each assignment's global rank is base + local rank, which decides kept / dropped
 // and the slot; perm and the slot weights are assembled in shared memory and written out
 // coalesced.
+//
+// Token-sharded batches (counts_all != null): this call holds one shard of a batch split
+// over ranks in token order, and counts_all [n_ranks, E] holds every shard's raw counts.
+// The assignments of earlier shards come first in the batch's token order, so expert e's
+// capacity left for this shard is max(0, C - sum over earlier shards of their counts), and
+// the kept / dropped decisions equal those of the whole batch dispatched at once.
 #include <algorithm>
 
 #include "launch.h"
@@ -47,12 +53,14 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
     const int32_t* __restrict__ topk_idx, int n, int k, int E, int C,
     int32_t* __restrict__ counts_raw, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm, int32_t* __restrict__ slot_of, const float* __restrict__ topk_w,
-    float* __restrict__ slot_w, int S_cap, int stage_out) {
+    float* __restrict__ slot_w, int S_cap, int stage_out, const int32_t* __restrict__ counts_all,
+    int rank) {
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;                       // [kWarps][E]: running count, then warp base
   int32_t* offs = sm + kWarps * E;         // [E + 1]
   int32_t* wsum = offs + E + 1;            // [kWarps] scan scratch
-  int32_t* perm_s = wsum + kWarps;         // [S_cap] when stage_out: perm, written out coalesced
+  int32_t* capv = wsum + kWarps;           // [E] capacity left for this call, per expert
+  int32_t* perm_s = capv + E;              // [S_cap] when stage_out: perm, written out coalesced
   float* slotw_s = reinterpret_cast<float*>(perm_s + S_cap);   // [S_cap] gate weight per slot
   const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -134,7 +142,14 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
       run += c;
     }
     counts_raw[e] = run;
-    my_kept = min(run, C);
+    int cap = C;
+    if (counts_all) {
+      int before = 0;                                   // earlier shards' assignments to e
+      for (int r = 0; r < rank; ++r) before += counts_all[(size_t)r * E + e];
+      cap = max(0, C - before);
+    }
+    capv[e] = cap;
+    my_kept = min(run, cap);
     kept[e] = my_kept;
   }
   // block-wide exclusive scan of my_kept over threads 0 .. E-1 (E <= 1024)
@@ -175,7 +190,7 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
       return;
     }
     const int r = cnt[w * E + e] + rank_local;
-    if (r < C) {
+    if (r < capv[e]) {
       const int s = offs[e] + r;
       slot_of[a] = s;
       if (stage_out) {
@@ -224,14 +239,17 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(
 
 }  // namespace
 
-size_t dispatch_smem_bytes(int E) { return sizeof(int32_t) * ((size_t)kWarps * E + E + 1 + kWarps); }
+size_t dispatch_smem_bytes(int E) {
+  return sizeof(int32_t) * ((size_t)kWarps * E + E + 1 + kWarps + E);
+}
 
 // Slots staged in shared memory when they fit beside the counters.
 constexpr size_t kDispatchSmemMax = 200 * 1024;
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C, int32_t* counts_raw,
                             int32_t* kept, int32_t* offsets, int32_t* perm, int32_t* slot_of,
-                            const float* topk_w, float* slot_w, cudaStream_t s, bool pdl) {
+                            const float* topk_w, float* slot_w, cudaStream_t s, bool pdl,
+                            const int32_t* counts_all, int rank) {
   const int n = T * k;
   const int S_cap = (int)std::min<long long>(n, (long long)E * C);
   size_t smem = dispatch_smem_bytes(E);
@@ -243,7 +261,7 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C,
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern));
   if (err != cudaSuccess) return err;
   return launch_k(kern, 1, kWarps * 32, smem, s, pdl, topk_idx, n, k, E, C, counts_raw, kept,
-                  offsets, perm, slot_of, topk_w, slot_w, S_cap, stage_out);
+                  offsets, perm, slot_of, topk_w, slot_w, S_cap, stage_out, counts_all, rank);
 }
 
 }  // namespace moe

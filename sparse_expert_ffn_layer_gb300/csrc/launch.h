@@ -92,7 +92,7 @@ size_t dispatch_smem_bytes(int E);
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C,
                             int32_t* counts_raw, int32_t* kept, int32_t* offsets, int32_t* perm,
                             int32_t* slot_of, const float* topk_w, float* slot_w, cudaStream_t s,
-                            bool pdl = false);
+                            bool pdl = false, const int32_t* counts_all = nullptr, int rank = 0);
 
 int gemm_stages_for(int nmax, int E, int mw, int smem_limit);
 // Raises the kernel's dynamic shared-memory limit to the device maximum, once per kernel

@@ -90,6 +90,16 @@ def test_argument_errors_return_before_any_launch(moe):
     assert L.moe_dispatch(P, 8, 4, 1, 1.0, None, P, P, P, P, s) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_dispatch(P, 8, 2000, 1, 1.0, P, P, P, P, P, s) == moe.MOE_ERR_UNSUPPORTED
     assert L.moe_dispatch(P, 0, 4, 1, 1.0, P, P, P, P, P, s) == moe.MOE_OK
+    # sharded dispatch: batch smaller than the shard, rank outside the ranks, counts missing
+    assert L.moe_dispatch_sharded(P, 8, 4, 1, 1.0, 4, P, 2, 0, P, P, P, P, P, s) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch_sharded(P, 8, 4, 1, 1.0, 16, P, 2, 2, P, P, P, P, P, s) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch_sharded(P, 8, 4, 1, 1.0, 16, None, 2, 1, P, P, P, P, P, s) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch_sharded(P, 8, 2000, 1, 1.0, 16, P, 2, 1, P, P, P, P, P, s) == \
+        moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_dispatch_sharded(P, 0, 4, 1, 1.0, 16, P, 2, 1, P, P, P, P, P, s) == moe.MOE_OK
     # expert ffn: unsupported shape, small workspace
     assert L.moe_expert_ffn(P, P, P, P, P, 1, 8, 100, 256, 4, 8, P, P, 1 << 20, s) == \
         moe.MOE_ERR_UNSUPPORTED

@@ -117,6 +117,60 @@ def test_dispatch_all_to_one_expert(m):
     assert np.all(slot[C:, 0] == -1) and np.array_equal(slot[:C, 0], np.arange(C))
 
 
+@pytest.mark.parametrize("T,E,k,cf,cuts", [(4096, 128, 1, 1.25, (0, 1000, 1000, 2500, 4096)),
+                                           (16384, 128, 2, 1.25, (0, 8192, 16384)),
+                                           (3000, 16, 2, 1.0, (0, 1, 1500, 2999, 3000)),
+                                           (999, 1024, 2, 2.0, (0, 333, 999))])
+def test_dispatch_sharded_bit_exact(m, T, E, k, cf, cuts):
+    """Token-sharded routing: each shard dispatched with the earlier shards' counts keeps
+    exactly what the whole batch keeps.  The ranks are emulated one after another on this GPU
+    (independent launches that never wait on one another); the counts exchange is a stack of
+    the shards' counts_raw."""
+    rng = np.random.default_rng(T + E)
+    p = 1.0 / np.arange(1, E + 1) ** 1.1
+    p /= p.sum()
+    if k == 1:
+        idx = rng.choice(E, size=(T, 1), p=p)
+    else:
+        idx = np.array([rng.choice(E, 2, replace=False, p=p) for _ in range(T)])
+    idx = idx.astype(np.int32)
+    R = len(cuts) - 1
+    shards = [torch.from_numpy(idx[cuts[r]:cuts[r + 1]].copy()).cuda() for r in range(R)]
+    counts = []
+    for r in range(R):
+        Tr = cuts[r + 1] - cuts[r]
+        c = torch.zeros(E, dtype=torch.int32, device="cuda")
+        if Tr:
+            z = lambda n: torch.empty(n, dtype=torch.int32, device="cuda")  # noqa: E731
+            m.moe_dispatch(shards[r], E, cf, c, z(E), z(E + 1), z(Tr * k),
+                           torch.empty((Tr, k), dtype=torch.int32, device="cuda"))
+        counts.append(c)
+    counts_all = torch.stack(counts).contiguous()
+    C = oracle.capacity(T, E, float(np.float32(cf)))
+    whole = oracle.dispatch(idx, E, C)
+    bases = oracle.shard_bases(counts_all.cpu().numpy())
+    assert np.array_equal(counts_all.cpu().numpy().sum(0), whole.counts_raw)
+    for r in range(R):
+        lo, hi = cuts[r], cuts[r + 1]
+        Tr = hi - lo
+        cnt = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+        kept = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+        offs = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda")
+        perm = torch.full((max(1, Tr * k),), -1, dtype=torch.int32, device="cuda")
+        slot = torch.full((Tr, k), -9, dtype=torch.int32, device="cuda")
+        m.moe_dispatch_sharded(shards[r], E, cf, T, counts_all, r, cnt, kept, offs, perm, slot)
+        torch.cuda.synchronize()
+        if Tr == 0:
+            continue
+        ref = oracle.dispatch_shard(idx[lo:hi], E, C, bases[r])
+        assert np.array_equal(cnt.cpu().numpy(), ref.counts_raw)
+        assert np.array_equal(kept.cpu().numpy(), ref.kept)
+        assert np.array_equal(offs.cpu().numpy(), ref.offsets)
+        assert np.array_equal(perm.cpu().numpy()[:ref.S], ref.perm)
+        assert np.array_equal(slot.cpu().numpy(), ref.slot_of)
+        assert np.array_equal(ref.slot_of >= 0, whole.slot_of[lo:hi] >= 0)
+
+
 # ------------------------------------------------------------------------------ whole layer
 LAYER_CASES = [
     ("tiny_fp32", 128, None), ("tiny_fp32", 1, None), ("tiny_fp32", 37, None),

@@ -1,5 +1,9 @@
-"""The N > 1 bench path on CPU ranks (gloo, world size 2): replicas time their own steps, the
-slowest rank defines the job time, and rank 0 alone reports."""
+"""Multi-rank host logic on CPU ranks (gloo).
+
+The N > 1 bench path (world size 2): replicas time their own steps, the slowest rank defines
+the job time, and rank 0 alone reports.  The token-sharded routing exchange (world size 3):
+each rank's expert counts reach every rank, and the oracle's shard dispatch with the
+resulting bases reproduces the whole batch's routing."""
 import os
 import socket
 
@@ -49,3 +53,66 @@ def test_reference_arm_only_rank0_reports(monkeypatch, capsys):
                               gpus=2))()
     assert bench.run_reference(args) is None
     assert capsys.readouterr().out == ""
+
+
+def _shard_rank_main(rank, world, port, q):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import oracle
+    from sparse_expert_ffn_layer_gb300 import sharded
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    rng = np.random.default_rng(11)
+    T, E, k = 301, 8, 2
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[:, 5] += 1.0                                        # a hot expert
+    _, idx, _ = oracle.softmax_topk(logits, k)
+    cuts = [0, 77, 77, T]                                     # rank 1 holds no tokens
+    lo, hi = cuts[rank], cuts[rank + 1]
+    mine = idx[lo:hi]
+    counts = torch.from_numpy(np.bincount(mine.reshape(-1), minlength=E).astype(np.int32))
+    counts_all, T_global = sharded.exchange_counts(counts, hi - lo)
+    C = oracle.capacity(T_global, E, 1.0)
+    base = oracle.shard_bases(counts_all.numpy())[rank]
+    got = oracle.dispatch_shard(mine, E, C, base)
+    q.put((rank, T_global, counts_all.numpy().tolist(), got.slot_of.tolist(),
+           got.perm.tolist(), got.offsets.tolist()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_sharded_routing_exchange_on_three_cpu_ranks():
+    import numpy as np
+
+    import oracle
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    world = 3
+    procs = [ctx.Process(target=_shard_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=180) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    rng = np.random.default_rng(11)
+    T, E, k = 301, 8, 2
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[:, 5] += 1.0
+    _, idx, _ = oracle.softmax_topk(logits, k)
+    whole = oracle.dispatch(idx, E, oracle.capacity(T, E, 1.0))
+    cuts = [0, 77, 77, T]
+    assert whole.kept.max() == oracle.capacity(T, E, 1.0)      # the cut binds somewhere
+    for rank, T_global, counts_all, slot_of, perm, offsets in res:
+        assert T_global == T
+        assert np.array_equal(np.array(counts_all).sum(0), whole.counts_raw)
+        lo, hi = cuts[rank], cuts[rank + 1]
+        slot_of = np.array(slot_of).reshape(hi - lo, k)
+        assert np.array_equal(slot_of >= 0, whole.slot_of[lo:hi] >= 0)
+        for e in range(E):
+            seg = np.array(perm[offsets[e]:offsets[e + 1]], dtype=np.int64) + lo
+            w = whole.perm[whole.offsets[e]:whole.offsets[e + 1]]
+            assert np.array_equal(seg, w[(w >= lo) & (w < hi)])
