@@ -10,7 +10,7 @@
  *   2. softmax       p[t,e] = exp(l[t,e] - max) / sum exp(.)    (double)
  *      top-k         k experts by logit, ties to the lower index
  *      gate weights  top-1: w = p[e1];  top-2: w_j = p_j / (p_1 + p_2)
- *   3. capacity      C = ceil(cf * T / E)
+ *   3. capacity      C = ceil(cf * T / E)   (cf = +infinity: C = T, dropless)
  *      dispatch      assignments (t, j) in token-major order; the rank of an
  *                    assignment is the number of earlier ones to the same
  *                    expert; kept iff rank < C; slots are compact:
@@ -126,9 +126,14 @@ void oracle_softmax_topk(const float* logits, int T, int E, int k, double* probs
   free(p);
 }
 
-/* Step 3a: capacity C = ceil(cf * T / E); -1 on bad arguments. */
+/*
+ * Step 3a: capacity C = ceil(cf * T / E); -1 on bad arguments.  cf = +infinity
+ * is the dropless mode: C = T, which no expert can exceed (a token's k experts
+ * are distinct), so nothing is dropped.
+ */
 int oracle_capacity(int T, int E, double cf) {
-  if (T < 1 || E < 1 || !(cf > 0.0) || isinf(cf)) return -1;
+  if (T < 1 || E < 1 || !(cf > 0.0)) return -1;
+  if (isinf(cf)) return T;
   double c = ceil(cf * (double)T / (double)E);
   if (c > 2147483647.0) return -1;
   return (int)c;

@@ -137,9 +137,20 @@ def test_capacity_closed_form(oracle_mod):
                 assert oracle_mod.capacity(T, E, cf) == math.ceil(q)
     assert oracle_mod.capacity(4096, 128, 1.25) == 40
     assert oracle_mod.capacity(16384, 128, 1.25) == 160
-    for bad in ((0, 4, 1.0), (4, 0, 1.0), (4, 4, 0.0), (4, 4, -1.0), (4, 4, float("inf")),
+    for bad in ((0, 4, 1.0), (4, 0, 1.0), (4, 4, 0.0), (4, 4, -1.0), (4, 4, float("-inf")),
                 (4, 4, float("nan"))):
         assert oracle_mod.capacity(*bad) == -1
+    # dropless (cf = +inf): C = T, so every assignment is kept however skewed the routing
+    for T, E in ((1, 4), (7, 3), (4096, 128)):
+        assert oracle_mod.capacity(T, E, float("inf")) == T
+    rng = np.random.default_rng(8)
+    for k in (1, 2):
+        T, E = 500, 6
+        idx = np.array([rng.choice(E, k, replace=False, p=[.7, .1, .1, .05, .03, .02])
+                        for _ in range(T)], np.int32)
+        dsp = oracle_mod.dispatch(idx, E, oracle_mod.capacity(T, E, float("inf")))
+        assert np.all(dsp.slot_of >= 0) and dsp.S == T * k
+        assert np.array_equal(dsp.kept, dsp.counts_raw)
 
 
 # ---------------------------------------------------------------- dispatch
