@@ -19,6 +19,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -47,12 +48,29 @@ def parse_args():
     p.add_argument("--tokens", type=int, default=4096)
     p.add_argument("--experts", type=int, default=None,
                    help="override the workload's expert count (smaller profiling cases)")
+    p.add_argument("--capacity-factor", type=float, default=None,
+                   help="override the workload's capacity factor; inf = dropless")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=20.0)
     p.add_argument("--no-graph", action="store_true",
                    help="launch each timed step directly instead of replaying its CUDA graph")
     return p.parse_args()
+
+
+def bench_config(args):
+    """The workload with the command line's overrides."""
+    cfg, T = synth.workload(args.workload, args.tokens)
+    if getattr(args, "experts", None):
+        cfg = cfg.at(E=args.experts)
+    if getattr(args, "capacity_factor", None) is not None:
+        cfg = cfg.at(cf=args.capacity_factor)
+    return cfg, T
+
+
+def cf_json(cf):
+    """The capacity factor as a JSON value (\"inf\" for the dropless mode)."""
+    return "inf" if math.isinf(cf) else cf
 
 
 def peaks():
@@ -176,7 +194,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    cfg, T = synth.workload(args.workload, args.tokens)
+    cfg, T = bench_config(args)
     K, W = args.steps, args.warmup
     r = OracleRunner(cfg, T, args.seed)
     n = r.size_for(min(5.0, 150.0 / max(1, K + W)))
@@ -194,7 +212,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": cfg.name, "T": T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
-                   "capacity_factor": cfg.cf},
+                   "capacity_factor": cf_json(cfg.cf)},
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": r.oracle.num_threads(),
                          "kind": "oracle", "sample": r.describe(n, K)},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -259,9 +277,7 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl")
 
-    cfg, T = synth.workload(args.workload, args.tokens)
-    if args.experts:
-        cfg = cfg.at(E=args.experts)
+    cfg, T = bench_config(args)
     seed = args.seed + 1000 * rank
     f16 = cfg.dtype == "f16"
     tdt = torch.float16 if f16 else torch.float32
@@ -444,7 +460,8 @@ def run_ours(args):
         "data": "synthetic (seeded counter-based draws; 4 token batches cycled)",
         "config": {"workload": f"{cfg.name}: 350M+MoE-128 layer" if cfg.name == "moe350m_e128"
                    else cfg.name, "T": T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
-                   "capacity_factor": cfg.cf, "mlp_type": "residual" if cfg.residual else "standard",
+                   "capacity_factor": cf_json(cfg.cf),
+                   "mlp_type": "residual" if cfg.residual else "standard",
                    "l2": f"inputs larger than L2: {2 * cfg.E * cfg.d * cfg.f * el / 1e9:.2f} GB of "
                          "expert weights per step vs 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

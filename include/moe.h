@@ -75,7 +75,11 @@ typedef enum { MOE_MLP_STANDARD = 0, MOE_MLP_RESIDUAL = 1 } moe_mlp_type;
  * Capacity per expert: C = ceil(cf * T / E), with cf*T and the division evaluated in
  * double.  The pages name an expert's capacity (DeepSpeed-MoE review, "Phenomenon2") but
  * give no formula; this is the capacity-factor definition.  Host only.
- * Returns C (0 when T = 0), or -1 when T < 0, E < 1, cf <= 0 / not finite, or C > 2^31-1.
+ * cf = +INFINITY selects the dropless mode: C = T, so no assignment is dropped and a hot
+ * expert's rows are spread over as many tiles as it needs (the single-GPU counterpart of the
+ * physical expert replicas of "Fast MoE Inference via Predictive Prefetching and Expert
+ * Replication", methodology).  Every entry taking a capacity factor accepts it.
+ * Returns C (0 when T = 0), or -1 when T < 0, E < 1, cf <= 0 or NaN, or C > 2^31-1.
  */
 MOE_API int moe_capacity(int T, int E, float capacity_factor);
 

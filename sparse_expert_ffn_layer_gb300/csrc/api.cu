@@ -19,8 +19,9 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int capacity_of(int T, int E, float cf) {
-  if (T < 0 || E < 1 || !(cf > 0.0f) || isinf(cf)) return -1;
+  if (T < 0 || E < 1 || !(cf > 0.0f)) return -1;
   if (T == 0) return 0;
+  if (isinf(cf)) return T;              // dropless: no expert receives more than T assignments
   double c = ceil((double)cf * (double)T / (double)E);
   if (c > 2147483647.0) return -1;
   return (int)c;

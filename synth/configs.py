@@ -45,6 +45,13 @@ CONFIGS = {
                              residual=True, f_res=8192, T_list=(64, 2048)),
     "prmoe_e128": LayerConfig("prmoe_e128", d=2048, f=8192, E=128, k=1, cf=1.0, dtype="f16",
                               residual=True, f_res=8192, T_list=(64, 2048)),
+    # Top2-MoE at the PR-MoE layer's shape (d 2048, f 8192, E 64 / 128): two routed experts in
+    # place of one routed expert plus the dense MLP, the comparison of the DeepSpeed-MoE review,
+    # "Phenomenon2"
+    "top2_e64": LayerConfig("top2_e64", d=2048, f=8192, E=64, k=2, cf=1.0, dtype="f16",
+                            T_list=(64, 2048)),
+    "top2_e128": LayerConfig("top2_e128", d=2048, f=8192, E=128, k=2, cf=1.0, dtype="f16",
+                             T_list=(64, 2048)),
     # 2.4B+MoE-128 layer, top-2 with normalised gate weights, uniform and Zipf(1.2) load
     "moe2p4b_e128_top2": LayerConfig("moe2p4b_e128_top2", d=3584, f=14336, E=128, k=2, cf=1.25,
                                      dtype="f16", T_list=(1, 32, 1024, 16384)),

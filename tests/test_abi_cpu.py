@@ -39,9 +39,15 @@ def test_capacity_matches_oracle(moe, oracle_mod):
             for cf in (0.5, 1.0, 1.25, 2.0, 3.7):
                 assert moe.moe_capacity(T, E, cf) == oracle_mod.capacity(T, E, float(np.float32(cf)))
     assert moe.moe_capacity(0, 8, 1.0) == 0
-    for bad in ((-1, 4, 1.0), (4, 0, 1.0), (4, 4, 0.0), (4, 4, -2.0), (4, 4, float("inf")),
+    for bad in ((-1, 4, 1.0), (4, 0, 1.0), (4, 4, 0.0), (4, 4, -2.0), (4, 4, float("-inf")),
                 (4, 4, float("nan"))):
         assert moe.moe_capacity(*bad) == -1
+    for T, E in ((1, 4), (4096, 128), (16384, 128)):             # dropless
+        assert moe.moe_capacity(T, E, float("inf")) == T == oracle_mod.capacity(T, E, float("inf"))
+    # dropless workspace: S_max = T k slots of H
+    ws_drop = moe.moe_workspace_size(4096, 1024, 4096, 128, 2, float("inf"), 0, 0, 1)
+    ws_cap = moe.moe_workspace_size(4096, 1024, 4096, 128, 2, 1.0, 0, 0, 1)
+    assert ws_drop - ws_cap >= (2 * 4096 - 128 * 32) * 4096 * 2
 
 
 def test_workspace_size(moe):

@@ -180,6 +180,7 @@ LAYER_CASES = [
     ("prmoe_e64", 64, 24), ("prmoe_e128", 64, 24),
     ("moe2p4b_e128_top2", 1, None), ("moe2p4b_e128_top2", 32, 10),
     ("moe2p4b_e128_top2_zipf", 32, 10),
+    ("top2_e64", 64, 24), ("top2_e128", 2048, 24),
 ]
 
 
@@ -238,6 +239,28 @@ def test_layer_forward_largest(m, name, T):
     r = case.routing()
     assert np.array_equal(idx, r.topk_idx) and np.array_equal(slot, r.disp.slot_of)
     rows = sample_rows(r, T, 6)
+    ok, err, bound = within_tol(out[rows], case.reference_rows(rows))
+    assert ok, f"max err {err:.3e} > bound {bound:.3e}"
+    del case
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,T", [("moe350m_e128", 512), ("moe1p3b_e128_zipf", 2048),
+                                    ("moe2p4b_e128_top2_zipf", 16384)])
+def test_layer_forward_dropless(m, name, T):
+    """Capacity factor +inf: nothing is dropped, and the hot experts' rows (thousands at the
+    Zipf(1.2) top-2 shape) spread over as many row tiles as they need."""
+    cfg = synth.CONFIGS[name].at(cf=float("inf"))
+    case = Case(cfg, T, seed=3)
+    out, idx, slot = case.forward(m)
+    r = case.routing()
+    assert r.disp.C == T and r.disp.S == T * cfg.k
+    assert np.all(slot >= 0)
+    assert np.array_equal(idx, r.topk_idx) and np.array_equal(slot, r.disp.slot_of)
+    hot = int(np.argmax(r.disp.kept))
+    hot_tokens = r.disp.perm[r.disp.offsets[hot]:r.disp.offsets[hot + 1]]
+    rows = np.unique(np.concatenate([sample_rows(r, T, 6),
+                                     hot_tokens[[0, len(hot_tokens) // 2, -1]]])).astype(np.int32)
     ok, err, bound = within_tol(out[rows], case.reference_rows(rows))
     assert ok, f"max err {err:.3e} > bound {bound:.3e}"
     del case
