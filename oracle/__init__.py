@@ -253,3 +253,20 @@ def layer_forward(x, Wg, W1, W2, k, cf, Wr1=None, Wr2=None, logits_in=None, rows
     """The whole layer: returns (out [rows, d] float64, Routing)."""
     r = route(x, Wg, k, cf, logits_in)
     return combine_rows(x, r, W1, W2, Wr1, Wr2, rows), r
+
+
+def stack_forward(x, layers, k, cf):
+    """Layers chained in order (a PR-MoE style stack, DeepSpeed-MoE review, "PR-MoE: Pyramid-
+    Residual-MoE"): layer l's output, rounded once to the activation dtype of x, is layer
+    l+1's input.  layers: sequence of dicts with Wg, W1, W2 and, for residual layers, Wr1,
+    Wr2.  Returns (list of per-layer outputs in float64, list of per-layer inputs, list of
+    Routing)."""
+    h = _c(x)
+    outs, ins, routings = [], [], []
+    for L in layers:
+        ins.append(h)
+        out, r = layer_forward(h, L["Wg"], L["W1"], L["W2"], k, cf, L.get("Wr1"), L.get("Wr2"))
+        outs.append(out)
+        routings.append(r)
+        h = out.astype(x.dtype)
+    return outs, ins, routings

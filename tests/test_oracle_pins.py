@@ -422,6 +422,39 @@ def test_single_expert_reduces_to_mlp(oracle_mod):
     assert np.allclose(out, ref, rtol=1e-12, atol=1e-13)
 
 
+def test_stack_of_single_expert_layers_is_an_mlp_chain(oracle_mod):
+    """A stack of E = 1 layers (one with a residual MLP) is the plain chain of MLPs, with each
+    layer's output rounded to fp16 before the next layer; checked against torch float64."""
+    import torch
+    rng = np.random.default_rng(12)
+    T, d, f = 17, 16, 24
+    x = rng.standard_normal((T, d)).astype(np.float16)
+    layers = []
+    for l in range(3):
+        L = dict(Wg=rng.standard_normal((d, 1)).astype(np.float32),
+                 W1=(rng.standard_normal((1, d, f)) * 0.3).astype(np.float16),
+                 W2=(rng.standard_normal((1, f, d)) * 0.3).astype(np.float16))
+        if l == 1:
+            L["Wr1"] = (rng.standard_normal((d, f)) * 0.3).astype(np.float16)
+            L["Wr2"] = (rng.standard_normal((f, d)) * 0.3).astype(np.float16)
+        layers.append(L)
+    outs, ins, routings = oracle_mod.stack_forward(x, layers, 1, 1.0)
+    assert len(outs) == 3 and all((r.disp.slot_of >= 0).all() for r in routings)
+
+    def mlp(h, A, B):
+        g = torch.nn.functional.gelu(h @ torch.tensor(A.astype(np.float64)), approximate="tanh")
+        return g @ torch.tensor(B.astype(np.float64))
+
+    h = torch.tensor(x.astype(np.float64))
+    for l, L in enumerate(layers):
+        y = mlp(h, L["W1"][0], L["W2"][0])
+        if "Wr1" in L:
+            y = y + mlp(h, L["Wr1"], L["Wr2"])
+        assert np.allclose(outs[l], y.numpy(), rtol=1e-12, atol=1e-13), l
+        assert np.array_equal(ins[l], h.numpy().astype(np.float16))
+        h = torch.tensor(y.numpy().astype(np.float16).astype(np.float64))
+
+
 # ---------------------------------------------------------------- stored regression fixture
 def test_golden_tiny_fp32(oracle_mod):
     """Fixture written by tests/golden/make_golden.py (which calls only oracle/ and synth/)."""
