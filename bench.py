@@ -247,23 +247,6 @@ def traffic_record(kernel_file):
     return rec
 
 
-def count_graph_kernels(g):
-    """Kernel nodes of a captured step (from the graph's DOT dump), or None if unavailable."""
-    import tempfile
-    try:
-        with tempfile.TemporaryDirectory() as tmp:
-            path = os.path.join(tmp, "step.dot")
-            g.debug_dump(path)
-            text = open(path).read()
-        if os.environ.get("MOE_BENCH_DUMP_GRAPH"):
-            with open(os.environ["MOE_BENCH_DUMP_GRAPH"], "w") as fh:
-                fh.write(text)
-        names = [ln for ln in text.splitlines() if "KERNEL" in ln.upper() and "->" not in ln]
-        return len(names) or None
-    except Exception:
-        return None
-
-
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -344,10 +327,8 @@ def run_ours(args):
     # kernel.
     cap_stream = torch.cuda.Stream()
 
-    def capture(batch, events=None, debug=False):
+    def capture(batch, events=None):
         g = torch.cuda.CUDAGraph()
-        if debug and hasattr(g, "enable_debug_mode"):
-            g.enable_debug_mode()
         with torch.cuda.graph(g, stream=cap_stream):
             if events is not None:
                 moe.moe_set_stage_events(events)
@@ -355,7 +336,10 @@ def run_ours(args):
         moe.moe_set_stage_events(None)
         return g
 
-    plain = [] if args.no_graph else [capture(b, debug=(b == 0)) for b in range(n_batches)]
+    n0 = moe.moe_kernel_launches()
+    plain = [] if args.no_graph else [capture(b) for b in range(n_batches)]
+    # kernels per step: counted by the library at each launch while the graphs were captured
+    kernels_per_step = (moe.moe_kernel_launches() - n0) // n_batches if plain else None
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     props = torch.cuda.get_device_properties(local)
@@ -404,7 +388,6 @@ def run_ours(args):
         for j in range(moe.MOE_STAGE_EVENTS - 1):
             stage_ms[j] += evs[i][j].elapsed_time(evs[i][j + 1])
     stage_ms /= K
-    kernels_per_step = count_graph_kernels(plain[0]) if plain else None
 
     # end to end through the public API with host buffers: H2D tokens, forward, D2H output
     h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -451,7 +434,12 @@ def run_ours(args):
     layer_flops = 4.0 * cfg.d * cfg.f * S + 2.0 * T * cfg.d * cfg.E + \
         (4.0 * T * cfg.d * cfg.f_res if cfg.residual else 0.0)
     t_roof = max(layer_bytes / (hbm * 1e9), layer_flops / (bf16 * 1e12))
-    launches_per_step = kernels_per_step or 5 + (1 if (cfg.k == 2 or cfg.residual) else 0)
+    if kernels_per_step is None:         # direct launches: count one more step
+        n0 = moe.moe_kernel_launches()
+        step(dev_tok[0])
+        torch.cuda.synchronize()
+        kernels_per_step = moe.moe_kernel_launches() - n0
+    launches_per_step = kernels_per_step
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,

@@ -231,6 +231,14 @@ MOE_API moe_status moe_selftest_wait(void* workspace, uint64_t timeout_ns, moe_s
 MOE_API moe_status moe_set_stage_events(void* const* events, int n_events);
 
 /*
+ * Measurement hook (the pages have no counterpart): the number of kernels this library has
+ * enqueued in this process so far, counted on the host at each successful launch.  Inside a
+ * stream capture a launch is counted once when captured (not per graph replay), so the
+ * difference across a capture is the number of kernels per replay.  Never fails.
+ */
+MOE_API unsigned long long moe_kernel_launches(void);
+
+/*
  * Allocation-free variant of moe_expert_ffn (the pages have no counterpart).
  *
  * For callers that cannot allocate device memory where they run the layer: a plugin or

@@ -22,7 +22,7 @@ MOE_MLP_STANDARD, MOE_MLP_RESIDUAL = 0, 1
 EXPORTED = ("moe_capacity", "moe_workspace_size", "moe_gate_topk", "moe_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_status_read",
             "moe_status_string", "moe_selftest_wait", "moe_set_stage_events",
-            "moe_expert_ffn_noalloc", "moe_dispatch_sharded")
+            "moe_expert_ffn_noalloc", "moe_dispatch_sharded", "moe_kernel_launches")
 
 _lib = None
 MOE_STAGE_EVENTS = 7
@@ -54,6 +54,7 @@ def get_lib():
         "moe_set_stage_events": ([P, I], I),
         "moe_expert_ffn_noalloc": ([P, P, P, P, P, I, I, I, I, I, I, P, P], I),
         "moe_dispatch_sharded": ([P, I, I, I, F, I, P, I, I, P, P, P, P, P, P], I),
+        "moe_kernel_launches": ([], ctypes.c_ulonglong),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -97,6 +98,10 @@ def _dtype(t) -> int:
     if t.dtype == torch.float32:
         return MOE_F32
     raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def moe_kernel_launches() -> int:
+    return get_lib().moe_kernel_launches()
 
 
 def moe_capacity(T: int, E: int, capacity_factor: float) -> int:

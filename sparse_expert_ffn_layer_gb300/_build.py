@@ -15,8 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 SOURCES = ["api.cu", "gate.cu", "dispatch.cu", "grouped_gemm.cu", "simt_ffn.cu", "elementwise.cu",
-           "noalloc.cu"]
-HEADERS = ["common.cuh", "launch.h", os.path.join("..", "..", "include", "moe.h")]
+           "noalloc.cu", "route_small.cu"]
+HEADERS = ["common.cuh", "launch.h", "topk.cuh", os.path.join("..", "..", "include", "moe.h")]
 
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

@@ -408,7 +408,12 @@ cudaError_t ensure_smem_attr(const void* kernel) {
   int optin = 0;
   err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  cudaFuncAttributes fa;
+  err = cudaFuncGetAttributes(&fa, kernel);
+  if (err != cudaSuccess) return err;
+  // the limit covers dynamic shared memory only: leave room for the kernel's static part
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes);
   if (err == cudaSuccess) done.insert({kernel, dev});
   return err;
 }
@@ -459,6 +464,8 @@ moe_status expert_ffn_on_scratch(const void* tokens, const int32_t* perm, const 
 extern "C" {
 
 int moe_capacity(int T, int E, float capacity_factor) { return capacity_of(T, E, capacity_factor); }
+
+unsigned long long moe_kernel_launches(void) { return launch_counter().load(); }
 
 moe_status moe_workspace_size(int T, int d, int f, int E, int k, float capacity_factor,
                               moe_mlp_type mlp_type, int f_res, moe_dtype dtype, size_t* bytes) {
@@ -625,14 +632,25 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
   const int mode = (k == 1 && !residual) ? kModeDirect : kModeAccum;
   const int S_max = (int)std::min<long long>((long long)T * k, (long long)E * C);
 
+  // status word and, next to it, the fused router's arrival counter
+  unsigned int* route_counter = reinterpret_cast<unsigned int*>(ws + L.status + sizeof(int));
   MOE_TRY(stage_mark(0, s));
-  MOE_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
-  MOE_TRY(launch_gate_logits(tokens, f16, Wg, T, d, E, logits, s));
-  MOE_TRY(stage_mark(1, s));
-  MOE_TRY(launch_softmax_topk(logits, T, E, k, nullptr, topk_idx, topk_w, nullptr, s, use_pdl()));
-  MOE_TRY(stage_mark(2, s));
-  MOE_TRY(launch_dispatch(topk_idx, T, k, E, C, counts, kept, offsets, perm, slot_of, topk_w, slot_w,
-                          s, use_pdl()));
+  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
+  if (f16 && gate_route_small_ok(T, d, E, tokens, Wg)) {
+    // decode-sized batch: gate, top-k and dispatch in one launch
+    MOE_TRY(launch_gate_route_small(static_cast<const __half*>(tokens), Wg, T, d, E, k, C, logits,
+                                    topk_idx, topk_w, counts, kept, offsets, perm, slot_of, slot_w,
+                                    route_counter, s));
+    MOE_TRY(stage_mark(1, s));
+    MOE_TRY(stage_mark(2, s));
+  } else {
+    MOE_TRY(launch_gate_logits(tokens, f16, Wg, T, d, E, logits, s));
+    MOE_TRY(stage_mark(1, s));
+    MOE_TRY(launch_softmax_topk(logits, T, E, k, nullptr, topk_idx, topk_w, nullptr, s, use_pdl()));
+    MOE_TRY(stage_mark(2, s));
+    MOE_TRY(launch_dispatch(topk_idx, T, k, E, C, counts, kept, offsets, perm, slot_of, topk_w,
+                            slot_w, s, use_pdl()));
+  }
   MOE_TRY(stage_mark(3, s));
   const int rows_bound = std::max(std::min(C, T * k), residual ? T : 0);
   if (f16) {

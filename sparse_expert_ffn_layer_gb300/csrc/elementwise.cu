@@ -181,15 +181,15 @@ cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d
 }
 
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s) {
-  zero_f32_kernel<<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(p, n);
+  MOE_LAUNCH(launch_k(zero_f32_kernel, grid_for(n / 4 + 1, 256), 256, 0, s, false, p, n));
   return cudaGetLastError();
 }
 
 cudaError_t launch_zero_dropped_rows(const int32_t* slot_of, int T, int k, int d, int dtype_f16,
                                      void* out, cudaStream_t s) {
   const size_t row_bytes = (size_t)d * (dtype_f16 ? 2 : 4);
-  zero_dropped_rows_kernel<<<grid_for((size_t)T * 32, 256), 256, 0, s>>>(
-      slot_of, T, k, row_bytes, static_cast<uint8_t*>(out));
+  MOE_LAUNCH(launch_k(zero_dropped_rows_kernel, grid_for((size_t)T * 32, 256), 256, 0, s, false,
+                      slot_of, T, k, row_bytes, static_cast<uint8_t*>(out)));
   return cudaGetLastError();
 }
 
@@ -208,18 +208,19 @@ cudaError_t launch_combine(const void* expert_out, const int32_t* slot_of, const
                            cudaStream_t s) {
   const int g = grid_for((size_t)T * 32, 256);
   if (dtype_f16)
-    combine_kernel<__half><<<g, 256, 0, s>>>(static_cast<const __half*>(expert_out), slot_of, topk_w,
-                                             static_cast<const __half*>(residual_in), T, d, k,
-                                             static_cast<__half*>(out));
+    MOE_LAUNCH(launch_k(combine_kernel<__half>, g, 256, 0, s, false,
+                        static_cast<const __half*>(expert_out), slot_of, topk_w,
+                        static_cast<const __half*>(residual_in), T, d, k,
+                        static_cast<__half*>(out)));
   else
-    combine_kernel<float><<<g, 256, 0, s>>>(static_cast<const float*>(expert_out), slot_of, topk_w,
-                                            static_cast<const float*>(residual_in), T, d, k,
-                                            static_cast<float*>(out));
+    MOE_LAUNCH(launch_k(combine_kernel<float>, g, 256, 0, s, false,
+                        static_cast<const float*>(expert_out), slot_of, topk_w,
+                        static_cast<const float*>(residual_in), T, d, k, static_cast<float*>(out)));
   return cudaGetLastError();
 }
 
 cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s) {
-  selftest_wait_kernel<<<1, 32, 0, s>>>(status, timeout_ns);
+  MOE_LAUNCH(launch_k(selftest_wait_kernel, 1, 32, 0, s, false, status, timeout_ns));
   return cudaGetLastError();
 }
 

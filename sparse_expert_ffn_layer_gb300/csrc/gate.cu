@@ -6,6 +6,7 @@
 // thread owns whole outputs of a register tile and walks the shared dimension in order, so
 // the result is bit-identical to any IEEE evaluation of that chain and routing is exact.
 #include "launch.h"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -273,19 +274,9 @@ __global__ void __launch_bounds__(256) gate_logits_small_kernel(const Tin* __res
   if (t < T && e < E) logits[(size_t)t * E + e] = acc;
 }
 
-// (v, i) beats (w, j) when v > w, or v == w and i < j: descending logit, ties to lower index.
-__device__ __forceinline__ bool beats(float v, int i, float w, int j) {
-  return v > w || (v == w && i < j);
-}
-
-__device__ __forceinline__ void warp_argmax(float& v, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-    int i2 = __shfl_xor_sync(0xffffffffu, i, o);
-    if (beats(v2, i2, v, i)) { v = v2; i = i2; }
-  }
-}
+struct PlainLoad {
+  __device__ __forceinline__ float operator()(const float* p) const { return *p; }
+};
 
 // One warp per token: softmax over E (fp32) and top-k on the logits.
 __global__ void __launch_bounds__(256) softmax_topk_kernel(const float* __restrict__ logits, int T,
@@ -299,43 +290,13 @@ __global__ void __launch_bounds__(256) softmax_topk_kernel(const float* __restri
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float* l = logits + (size_t)t * E;
-  float v1 = -INFINITY;
-  int i1 = 0x7fffffff;
-  for (int e = lane; e < E; e += 32) {
-    float v = l[e];
-    if (logits_copy) logits_copy[(size_t)t * E + e] = v;
-    if (beats(v, e, v1, i1)) { v1 = v; i1 = e; }
-  }
-  warp_argmax(v1, i1);
-  float v2 = -INFINITY;
-  int i2 = 0x7fffffff;
-  if (k == 2) {
-    for (int e = lane; e < E; e += 32) {
-      float v = l[e];
-      if (e != i1 && beats(v, e, v2, i2)) { v2 = v; i2 = e; }
-    }
-    warp_argmax(v2, i2);
-  }
-  float s = 0.0f;
-  for (int e = lane; e < E; e += 32) s += expf(l[e] - v1);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (probs_out) {
-    float inv = 1.0f / s;
-    for (int e = lane; e < E; e += 32) probs_out[(size_t)t * E + e] = expf(l[e] - v1) * inv;
-  }
+  const TopK r = softmax_topk_warp(logits + (size_t)t * E, E, k, lane, PlainLoad(),
+                                   probs_out ? probs_out + (size_t)t * E : nullptr,
+                                   logits_copy ? logits_copy + (size_t)t * E : nullptr);
   if (lane == 0) {
-    if (k == 1) {
-      topk_idx[t] = i1;
-      topk_w[t] = 1.0f / s;                         // p[e1] = exp(0) / sum
-    } else {
-      float r = expf(v2 - v1);                      // p2 / p1
-      float z = 1.0f + r;
-      topk_idx[2 * t] = i1;
-      topk_idx[2 * t + 1] = i2;
-      topk_w[2 * t] = 1.0f / z;
-      topk_w[2 * t + 1] = r / z;
+    for (int j = 0; j < k; ++j) {
+      topk_idx[(size_t)t * k + j] = r.idx[j];
+      topk_w[(size_t)t * k + j] = r.w[j];
     }
   }
 }
@@ -350,12 +311,12 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
     dim3 g((E + kSExp - 1) / kSExp, (T + kSTok - 1) / kSTok);
     if (dtype_f16) {
       const size_t smem = kSStages * small_slot_bytes<__half>();
-      gate_logits_small_kernel<__half><<<g, 256, smem, s>>>(static_cast<const __half*>(x), Wg, T, d,
-                                                            E, logits);
+      MOE_LAUNCH(launch_k(gate_logits_small_kernel<__half>, g, 256, smem, s, false,
+                          static_cast<const __half*>(x), Wg, T, d, E, logits));
     } else {
       const size_t smem = kSStages * small_slot_bytes<float>();
-      gate_logits_small_kernel<float><<<g, 256, smem, s>>>(static_cast<const float*>(x), Wg, T, d, E,
-                                                           logits);
+      MOE_LAUNCH(launch_k(gate_logits_small_kernel<float>, g, 256, smem, s, false,
+                          static_cast<const float*>(x), Wg, T, d, E, logits));
     }
     return cudaGetLastError();
   }
@@ -365,12 +326,16 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
                    (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
   if (dtype_f16) {
     const __half* xh = static_cast<const __half*>(x);
-    if (vec) gate_logits_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
-    else gate_logits_scalar_kernel<__half><<<grid, 256, 0, s>>>(xh, Wg, T, d, E, logits);
+    if (vec) MOE_LAUNCH(launch_k(gate_logits_kernel<__half>, grid, 256, 0, s, false, xh, Wg, T, d,
+                                 E, logits));
+    else MOE_LAUNCH(launch_k(gate_logits_scalar_kernel<__half>, grid, 256, 0, s, false, xh, Wg, T,
+                             d, E, logits));
   } else {
     const float* xf = static_cast<const float*>(x);
-    if (vec) gate_logits_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
-    else gate_logits_scalar_kernel<float><<<grid, 256, 0, s>>>(xf, Wg, T, d, E, logits);
+    if (vec) MOE_LAUNCH(launch_k(gate_logits_kernel<float>, grid, 256, 0, s, false, xf, Wg, T, d, E,
+                                 logits));
+    else MOE_LAUNCH(launch_k(gate_logits_scalar_kernel<float>, grid, 256, 0, s, false, xf, Wg, T, d,
+                             E, logits));
   }
   return cudaGetLastError();
 }

@@ -1,11 +1,18 @@
 // Internal interface between the C-ABI front end (api.cu) and the kernels.
 #pragma once
 
+#include <atomic>
 #include <utility>
 
 #include "common.cuh"
 
 namespace moe {
+
+// Kernels this library has enqueued in the process (inside a stream capture: captured).
+inline std::atomic<unsigned long long>& launch_counter() {
+  static std::atomic<unsigned long long> n{0};
+  return n;
+}
 
 // Launches `kernel`; with pdl the launch carries programmatic stream serialisation, so the
 // grid may start while the previous kernel of the stream finishes (the kernel itself waits
@@ -23,8 +30,16 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (err == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+  return err;
 }
+
+#define MOE_LAUNCH(expr)                     \
+  do {                                       \
+    const cudaError_t e_ = (expr);           \
+    if (e_ != cudaSuccess) return e_;        \
+  } while (0)
 
 // Epilogue kinds of the grouped GEMM.
 enum : int { kEpiGeluH = 0, kEpiCombine = 1 };
@@ -89,6 +104,13 @@ cudaError_t launch_softmax_topk(const float* logits, int T, int E, int k, float*
                                 int32_t* topk_idx, float* topk_w, float* logits_copy,
                                 cudaStream_t s, bool pdl = false);
 size_t dispatch_smem_bytes(int E);
+// Fused gate + top-k + dispatch for T <= 64 (route_small.cu); *counter must be 0 at launch.
+bool gate_route_small_ok(int T, int d, int E, const void* x, const void* Wg);
+cudaError_t launch_gate_route_small(const __half* x, const float* Wg, int T, int d, int E, int k,
+                                    int C, float* logits, int32_t* topk_idx, float* topk_w,
+                                    int32_t* counts_raw, int32_t* kept, int32_t* offsets,
+                                    int32_t* perm, int32_t* slot_of, float* slot_w,
+                                    unsigned int* counter, cudaStream_t s);
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int k, int E, int C,
                             int32_t* counts_raw, int32_t* kept, int32_t* offsets, int32_t* perm,
                             int32_t* slot_of, const float* topk_w, float* slot_w, cudaStream_t s,

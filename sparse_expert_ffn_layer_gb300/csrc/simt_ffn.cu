@@ -97,13 +97,13 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs a) {
 cudaError_t launch_simt_ffn1(const SimtArgs& a, int rows_bound, cudaStream_t s) {
   const int cols = max(a.f, a.Wr1 ? a.f_res : 0);
   dim3 grid((cols + kC - 1) / kC, a.E + (a.Wr1 ? 1 : 0), (rows_bound + kR - 1) / kR);
-  simt_gemm_kernel<1><<<grid, 256, 0, s>>>(a);
+  MOE_LAUNCH(launch_k(simt_gemm_kernel<1>, grid, 256, 0, s, false, a));
   return cudaGetLastError();
 }
 
 cudaError_t launch_simt_ffn2(const SimtArgs& a, int rows_bound, cudaStream_t s) {
   dim3 grid((a.d + kC - 1) / kC, a.E + (a.Wr2 ? 1 : 0), (rows_bound + kR - 1) / kR);
-  simt_gemm_kernel<2><<<grid, 256, 0, s>>>(a);
+  MOE_LAUNCH(launch_k(simt_gemm_kernel<2>, grid, 256, 0, s, false, a));
   return cudaGetLastError();
 }
 
