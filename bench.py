@@ -48,6 +48,9 @@ def parse_args():
     p.add_argument("--tokens", type=int, default=4096)
     p.add_argument("--experts", type=int, default=None,
                    help="override the workload's expert count (smaller profiling cases)")
+    p.add_argument("--stack", default=None,
+                   help="time a pyramid stack of layers (a name in synth.STACKS) under one CUDA "
+                        "graph instead of one layer; --tokens tokens per step")
     p.add_argument("--capacity-factor", type=float, default=None,
                    help="override the workload's capacity factor; inf = dropless")
     p.add_argument("--seed", type=int, default=0)
@@ -479,10 +482,153 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_stack(args):
+    """A pyramid stack of layers chained through device buffers, one CUDA graph per token
+    batch covering every layer; value = tokens through the whole stack per second."""
+    import torch
+
+    import sparse_expert_ffn_layer_gb300 as moe
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    names = synth.STACKS[args.stack]
+    cfgs = [synth.CONFIGS[n] for n in names]
+    if args.capacity_factor is not None:
+        cfgs = [c.at(cf=args.capacity_factor) for c in cfgs]
+    T, d = args.tokens, cfgs[0].d
+    assert all(c.d == d and c.dtype == "f16" for c in cfgs)
+    layers = []
+    for l, c in enumerate(cfgs):
+        sd = synth.layer_seed(args.seed, l)
+        L = {"W1": torch.empty((c.E, c.d, c.f), dtype=torch.float16, device="cuda"),
+             "W2": torch.empty((c.E, c.f, c.d), dtype=torch.float16, device="cuda")}
+        synth.fill_cuda(L["W1"], sd, synth.TID_W1, c.w_sigma)
+        synth.fill_cuda(L["W2"], sd, synth.TID_W2, c.w_sigma)
+        L["Wg"] = torch.from_numpy(synth.fill((c.d, c.E), synth.F32, sd, synth.TID_WG, c.w_sigma,
+                                              col_scale=synth.gate_col_scale(c, sd))).cuda()
+        L["Wr1"] = L["Wr2"] = None
+        if c.residual:
+            L["Wr1"] = torch.empty((c.d, c.f_res), dtype=torch.float16, device="cuda")
+            L["Wr2"] = torch.empty((c.f_res, c.d), dtype=torch.float16, device="cuda")
+            synth.fill_cuda(L["Wr1"], sd, synth.TID_WR1, c.w_sigma)
+            synth.fill_cuda(L["Wr2"], sd, synth.TID_WR2, c.w_sigma)
+        layers.append(L)
+    n_batches = 4
+    x = [torch.from_numpy(synth.fill((T, d), synth.F16, args.seed, synth.TID_TOKENS + (b << 8),
+                                     1.0)).cuda() for b in range(n_batches)]
+    bufs = [torch.empty((T, d), dtype=torch.float16, device="cuda") for _ in range(2)]
+    ws = torch.empty(max(moe.moe_workspace_size(T, c.d, c.f, c.E, c.k, c.cf,
+                                                1 if c.residual else 0, c.f_res, moe.MOE_F16)
+                         for c in cfgs), dtype=torch.uint8, device="cuda")
+    idx = [torch.empty((T, c.k), dtype=torch.int32, device="cuda") for c in cfgs]
+    slot = [torch.empty((T, c.k), dtype=torch.int32, device="cuda") for c in cfgs]
+
+    def run(b, events=None, stats=False):
+        for l, c in enumerate(cfgs):
+            L = layers[l]
+            src = x[b] if l == 0 else bufs[(l - 1) % 2]
+            if events is not None:
+                moe.moe_set_stage_events(events[l])
+            moe.moe_layer_forward(src, L["Wg"], L["W1"], L["W2"], c.k, c.cf, bufs[l % 2], ws,
+                                  mlp_type=1 if c.residual else 0, Wr1=L["Wr1"], Wr2=L["Wr2"],
+                                  topk_idx_out=idx[l] if stats else None,
+                                  slot_of_out=slot[l] if stats else None)
+        moe.moe_set_stage_events(None)
+
+    # routing statistics per layer (active experts) for the algorithmic bytes
+    active = np.zeros(len(cfgs))
+    for b in range(n_batches):
+        run(b, stats=True)
+        for l in range(len(cfgs)):
+            s_np, i_np = slot[l].cpu().numpy(), idx[l].cpu().numpy()
+            active[l] += len(np.unique(i_np[s_np >= 0])) / n_batches
+    if moe.moe_status_read(ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after the routing pass")
+    cap = torch.cuda.Stream()
+    n0 = moe.moe_kernel_launches()
+    graphs = []
+    for b in range(n_batches):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            run(b)
+        graphs.append(g)
+    kernels_per_step = (moe.moe_kernel_launches() - n0) // n_batches
+    for i in range(max(3, args.warmup)):
+        graphs[i % n_batches].replay()
+    torch.cuda.synchronize()
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else uuid
+    clocks = ClockSampler(gpu_id if gpu_id else "0")
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(K):
+        graphs[i % n_batches].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    clocks.stop()
+    if moe.moe_status_read(ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after the timed region")
+    ms = e0.elapsed_time(e1) / K
+    # per-layer times: replays of a graph carrying stage events around every layer
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_STAGE_EVENTS)]
+           for _ in cfgs]
+    for ev_l in evs:
+        for ev in ev_l:
+            ev.record(stream)
+    torch.cuda.synchronize()
+    gs = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gs, stream=cap):
+        run(0, events=evs)
+    reps = min(K, 20)
+    layer_ms = np.zeros(len(cfgs))
+    for _ in range(reps):
+        gs.replay()
+        torch.cuda.synchronize()
+        layer_ms += [ev_l[0].elapsed_time(ev_l[-1]) for ev_l in evs]
+    layer_ms /= reps
+    hbm, bf16, _, peak_src = peaks()
+    el = 2
+    bytes_total = 0.0
+    for l, c in enumerate(cfgs):
+        bytes_total += active[l] * 2 * c.d * c.f * el + c.d * c.E * 4 + 2 * T * c.d * el
+        if c.residual:
+            bytes_total += 2 * c.d * c.f_res * el
+    t_roof_ms = bytes_total / (hbm * 1e9) * 1e3
+    line = {
+        "metric": "PR-MoE stack tokens/sec on 1 GB300 (all layers per token) and % of HBM roofline",
+        "value": T / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic (seeded counter-based draws; 4 token batches cycled)",
+        "config": {"workload": args.stack, "layers": list(names), "T": T,
+                   "capacity_factor": cf_json(cfgs[0].cf),
+                   "l2": "inputs larger than L2: every layer's weights are distinct",
+                   "parallelism": "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": bytes_total / (ms / 1000.0) / 1e9, "peak": hbm,
+                     "unit": "GB/s", "frac": t_roof_ms / ms, "traffic": None,
+                     "kernel": "whole stack (algorithmic bytes of every layer / step time)",
+                     "peak_source": peak_src},
+        "layer_ms": [float(v) for v in layer_ms],
+        "active_experts": [float(v) for v in active],
+        "gpu_launches": K * kernels_per_step,
+        "launch": "one CUDA graph per step covering every layer, replayed back to back",
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.stack:
+        run_stack(args)
     else:
         run_ours(args)
 

@@ -21,7 +21,7 @@ import subprocess
 
 import numpy as np
 
-from .configs import CONFIGS, LayerConfig, workload  # noqa: F401
+from .configs import CONFIGS, STACKS, LayerConfig, layer_seed, workload  # noqa: F401
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 HOST_LIB = os.path.join(HERE, "libsynth_host.so")

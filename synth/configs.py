@@ -52,6 +52,14 @@ CONFIGS = {
                             T_list=(64, 2048)),
     "top2_e128": LayerConfig("top2_e128", d=2048, f=8192, E=128, k=2, cf=1.0, dtype="f16",
                              T_list=(64, 2048)),
+    # small PR-MoE layers for the stack parity test (dropless, so tokens do not interact);
+    # weights ~ N(0, 1/d) keep activations of order one through the chain
+    "tiny_prmoe_e8": LayerConfig("tiny_prmoe_e8", d=256, f=512, E=8, k=1, cf=float("inf"),
+                                 dtype="f16", residual=True, f_res=512, w_sigma=0.0625,
+                                 T_list=(64,)),
+    "tiny_prmoe_e16": LayerConfig("tiny_prmoe_e16", d=256, f=512, E=16, k=1, cf=float("inf"),
+                                  dtype="f16", residual=True, f_res=512, w_sigma=0.0625,
+                                  T_list=(64,)),
     # 2.4B+MoE-128 layer, top-2 with normalised gate weights, uniform and Zipf(1.2) load
     "moe2p4b_e128_top2": LayerConfig("moe2p4b_e128_top2", d=3584, f=14336, E=128, k=2, cf=1.25,
                                      dtype="f16", T_list=(1, 32, 1024, 16384)),
@@ -59,6 +67,21 @@ CONFIGS = {
                                           cf=1.25, dtype="f16", zipf=1.2,
                                           T_list=(1, 32, 1024, 16384)),
 }
+
+
+# Pyramid stacks (DeepSpeed-MoE review, "PR-MoE: Pyramid-Residual-MoE for Smaller Model Size
+# and Fast Inference": more experts in the last layers, an MLP beside every MoE module).  The
+# pages give neither the depth nor the split; the reading here: 12 MoE layers, the last two
+# with twice the experts, as in a 24-layer model with an MoE FFN in every other layer.
+STACKS = {
+    "prmoe_pyramid_12": ("prmoe_e64",) * 10 + ("prmoe_e128",) * 2,
+    "tiny_pyramid_3": ("tiny_prmoe_e8", "tiny_prmoe_e8", "tiny_prmoe_e16"),
+}
+
+
+def layer_seed(seed: int, layer: int) -> int:
+    """Seed of one layer's weights in a stack: distinct weights per layer."""
+    return seed * 1000 + 7919 * (layer + 1)
 
 
 def workload(name: str, T: int | None = None, **overrides) -> tuple[LayerConfig, int]:
