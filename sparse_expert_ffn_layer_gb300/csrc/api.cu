@@ -231,12 +231,28 @@ int choose_mw(long long row_tiles, int M_exp, long long res_tiles, int M_res, co
   return 1;
 }
 
-// Chunks per tile so that a launch has about four waves of work items, each chunk keeping at
-// least two 64-wide K blocks.
-int choose_ksplit(long long items_bound, int nkb_min, int sms) {
-  int ks = 1;
-  while (ks * 2 <= kMaxSplit && items_bound * ks < 4LL * sms && nkb_min / (ks * 2) >= 2) ks *= 2;
-  return ks;
+// Decode-sized batches: weight blocks per item (mw) and K chunks per item (ks) together.
+// All work units (items x chunks) should run in one round, one per CTA; the widest mw that
+// still spreads the weights over at least half the SMs wins (measured: wider items keep more
+// bytes in flight per CTA and beat narrower ones that fill every SM); a chunk keeps at least
+// two 64-wide K blocks.  mw candidates must divide every group's M and fit TMEM and three stages.
+void choose_split(long long row_tiles, int M_exp, long long res_tiles, int M_res, int nkb_min,
+                  const TcPlan& p, int E, int* mw_out, int* ks_out) {
+  int best = -1;
+  for (int mw = 4; mw >= 1; mw /= 2) {
+    if (M_exp % (128 * mw) || (res_tiles && M_res % (128 * mw))) continue;
+    if (mw > 1 && (nbuf_for(mw, p.acc_cols) == 0 || gemm_stages_for(p.nmax, E, mw, p.smem_optin) < 3))
+      continue;
+    const long long items = row_tiles * (M_exp / (128 * mw)) + res_tiles * (M_res / (128 * mw));
+    int ks = 1;
+    while (ks * 2 <= kMaxSplit && items * ks * 2 <= p.grid && nkb_min / (ks * 2) >= 2) ks *= 2;
+    const int score = (int)std::min<long long>(items * ks, p.grid / 2);
+    if (score > best) {
+      best = score;
+      *mw_out = mw;
+      *ks_out = ks;
+    }
+  }
 }
 
 // A (M-major weights) descriptor offsets for the 128-byte swizzle layout that two 64-wide
@@ -305,14 +321,13 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   const long long res1 = residual ? (T + plan1.nmax - 1) / plan1.nmax : 0;
   const long long tiles2 = std::min(E, S_rows) + S_rows / plan2.nmax;
   const long long res2 = residual ? (T + plan2.nmax - 1) / plan2.nmax : 0;
-  const int mw1 = choose_mw(tiles1, f, res1, f_res, plan1, E);
-  const int mw2 = choose_mw(tiles2, d, res2, d, plan2, E);
+  int mw1 = choose_mw(tiles1, f, res1, f_res, plan1, E);
+  int mw2 = choose_mw(tiles2, d, res2, d, plan2, E);
   int ks1 = 1, ks2 = 1;
   if (partial) {
-    ks1 = choose_ksplit(tiles1 * (f / 128 / mw1) + res1 * (residual ? f_res / 128 / mw1 : 0),
-                        d / 64, plan1.grid);
-    ks2 = choose_ksplit((tiles2 + res2) * (d / 128 / mw2),
-                        residual ? std::min(f, f_res) / 64 : f / 64, plan2.grid);
+    choose_split(tiles1, f, res1, f_res, d / 64, plan1, E, &mw1, &ks1);
+    choose_split(tiles2, d, res2, d, residual ? std::min(f, f_res) / 64 : f / 64, plan2, E, &mw2,
+                 &ks2);
     const size_t cols1 = std::max(f, residual ? f_res : 0);
     if ((size_t)ks1 * part_rows * cols1 * 4 > partial_bytes) ks1 = 1;
     if ((size_t)ks2 * part_rows * d * 4 > partial_bytes) ks2 = 1;

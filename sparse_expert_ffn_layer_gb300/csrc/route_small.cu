@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(kRThreads) gate_route_small_kernel(const Route
   const int e0 = blockIdx.x * kRExp, t0 = blockIdx.y * kRTok;
   const int nT = min(kRTok, a.T - t0);
   const int nch = a.d / kRKC;
+  // a warp holds tokens 4w .. 4w+3: warps past the batch's last token only help load
+  const bool computes = (tt & ~3) < nT;
 
   auto issue = [&](int c) {
     uint8_t* base = sm + (size_t)(c % kRStages) * kRStageBytes;
@@ -102,15 +104,17 @@ __global__ void __launch_bounds__(kRThreads) gate_route_small_kernel(const Route
     const uint8_t* base = sm + (size_t)(c % kRStages) * kRStageBytes;
     const float* ws = reinterpret_cast<const float*>(base) + ee;
     const __half* xs = reinterpret_cast<const __half*>(base + kRWBytes) + tt * kRXPitch;
+    if (computes) {
 #pragma unroll 4
-    for (int i = 0; i < kRKC; i += 8) {               // ascending i
-      const uint4 raw = *reinterpret_cast<const uint4*>(xs + i);
-      const __half2* h = reinterpret_cast<const __half2*>(&raw);
+      for (int i = 0; i < kRKC; i += 8) {             // ascending i
+        const uint4 raw = *reinterpret_cast<const uint4*>(xs + i);
+        const __half2* h = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __half22float2(h[q]);        // exact widening
-        acc = __fmaf_rn(f.x, ws[(i + 2 * q) * kRExp], acc);
-        acc = __fmaf_rn(f.y, ws[(i + 2 * q + 1) * kRExp], acc);
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __half22float2(h[q]);      // exact widening
+          acc = __fmaf_rn(f.x, ws[(i + 2 * q) * kRExp], acc);
+          acc = __fmaf_rn(f.y, ws[(i + 2 * q + 1) * kRExp], acc);
+        }
       }
     }
     __syncthreads();                                  // the slot may be refilled next
