@@ -39,20 +39,7 @@ constexpr int kSplitRows = 64;
 struct Ws {
   size_t status, logits, topk_idx, topk_w, counts, kept, offsets, perm, slot_w, slot_of, H, Hres,
       acc32, r32, partial, partial_bytes, total;
-  size_t ctrl_bytes;         // status word, router counter, split-K counters: cleared per call
-  size_t split_cnt1, split_cnt2;   // byte offsets of the two GEMMs' split-K counters
 };
-
-// Work items (before the K split) a grouped GEMM of a decode-sized batch can have at most:
-// row tiles of at least 16 rows over min(E, S) experts and S slots, plus the residual group's,
-// times the 128-row blocks of M.  One split-K counter per item.
-void split_counter_bounds(int T, int d, int f, int E, size_t S_max, bool residual, int f_res,
-                          size_t* n1, size_t* n2) {
-  const size_t tiles = std::min<size_t>((size_t)E, S_max) + S_max / 16;
-  const size_t res = residual ? ((size_t)T + 15) / 16 : 0;
-  *n1 = tiles * (size_t)(f / 128) + res * (size_t)(f_res / 128);
-  *n2 = (tiles + res) * (size_t)(d / 128);
-}
 
 Ws ws_layout(int T, int d, int f, int E, int k, int C, bool residual, int f_res, bool f16) {
   const size_t elt = f16 ? 2 : 4;
@@ -65,14 +52,7 @@ Ws ws_layout(int T, int d, int f, int E, int k, int C, bool residual, int f_res,
     off += align_up(bytes);
     return at;
   };
-  const size_t part_rows = S_max + (residual ? (size_t)T : 0);
-  const bool split = f16 && part_rows <= (size_t)kSplitRows;
-  size_t n1 = 0, n2 = 0;
-  if (split) split_counter_bounds(T, d, f, E, S_max, residual, f_res, &n1, &n2);
-  w.ctrl_bytes = split ? 16 + 4 * (n1 + n2) : 2 * sizeof(int);
-  w.split_cnt1 = 16;
-  w.split_cnt2 = 16 + 4 * n1;
-  w.status = take(std::max<size_t>(kAlign, w.ctrl_bytes));
+  w.status = take(kAlign);
   w.H = take(std::max<size_t>(S_max, 1) * f * elt);
   w.logits = take((size_t)T * E * 4);
   w.topk_idx = take((size_t)T * k * 4);
@@ -86,9 +66,10 @@ Ws ws_layout(int T, int d, int f, int E, int k, int C, bool residual, int f_res,
   w.Hres = residual ? take((size_t)T * f_res * elt) : 0;
   w.acc32 = accum ? take((size_t)T * d * 4) : 0;
   w.r32 = residual ? take((size_t)T * d * 4) : 0;
+  const size_t part_rows = S_max + (residual ? (size_t)T : 0);
   w.partial_bytes = 0;
   w.partial = 0;
-  if (split) {
+  if (f16 && part_rows <= (size_t)kSplitRows) {
     const size_t cols = std::max<size_t>(std::max(f, d), residual ? f_res : 0);
     w.partial_bytes = (size_t)kMaxSplit * part_rows * cols * 4;
     w.partial = take(w.partial_bytes);
@@ -326,8 +307,7 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
                       int d, int f, int E, int f_res, int S_rows, int rows_bound, __half* H,
                       __half* Hres, int mode, void* out, float* acc32, float* r32,
                       const float* slot_w, const int32_t* drop_slot_of, float* partial,
-                      size_t partial_bytes, unsigned int* split_cnt1, unsigned int* split_cnt2,
-                      int* status, bool pdl_first, cudaStream_t s) {
+                      size_t partial_bytes, int* status, bool pdl_first, cudaStream_t s) {
   const bool residual = Wr1 != nullptr;
   const bool pdl = use_pdl();
   // first GEMM: tiles of at most 64 token rows, so that items can span four weight blocks and
@@ -349,8 +329,8 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
     choose_split(tiles2, d, res2, d, residual ? std::min(f, f_res) / 64 : f / 64, plan2, E, &mw2,
                  &ks2);
     const size_t cols1 = std::max(f, residual ? f_res : 0);
-    if ((size_t)ks1 * part_rows * cols1 * 4 > partial_bytes || !split_cnt1) ks1 = 1;
-    if ((size_t)ks2 * part_rows * d * 4 > partial_bytes || !split_cnt2) ks2 = 1;
+    if ((size_t)ks1 * part_rows * cols1 * 4 > partial_bytes) ks1 = 1;
+    if ((size_t)ks2 * part_rows * d * 4 > partial_bytes) ks2 = 1;
   }
   CUtensorMap mW1, mX, mWr1, mW2, mH, mWr2, mHres;
   const int S_dim = std::max(S_rows, 1);
@@ -396,8 +376,8 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   g1.part_rows = part_rows;
   g1.part_cols = std::max(f, residual ? f_res : 0);
   g1.part_res_row0 = S_rows;
-  g1.split_cnt = split_cnt1;
   MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan1.grid, s, pdl && pdl_first));
+  if (ks1 > 1) MOE_TRY(launch_splitk_reduce1(g1, S_rows, T_res, f, f_res, s, pdl));
   MOE_TRY(stage_mark(4, s));
 
   GemmArgs g2;
@@ -422,8 +402,8 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   g2.part_rows = part_rows;
   g2.part_cols = d;
   g2.part_res_row0 = S_rows;
-  g2.split_cnt = split_cnt2;
   MOE_TRY(launch_grouped_gemm2(mW2, mH, mWr2, mHres, g2, plan2.grid, s, pdl));
+  if (ks2 > 1) MOE_TRY(launch_splitk_reduce2(g2, S_rows, T_res, d, s, pdl));
   MOE_TRY(stage_mark(5, s));
   return MOE_OK;
 }
@@ -476,8 +456,7 @@ moe_status expert_ffn_on_scratch(const void* tokens, const int32_t* perm, const 
   if (dtype == MOE_F16) {
     return run_tc_ffn(tokens, perm, offsets, W1, W2, nullptr, nullptr, T, d, f, E, 0, S_max, S_max,
                       reinterpret_cast<__half*>(scratch), nullptr, kModeExpertOut, expert_out,
-                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr, status,
-                      /*pdl_first=*/false, s);
+                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, /*pdl_first=*/false, s);
   }
   SimtArgs a;
   memset(&a, 0, sizeof(a));
@@ -596,8 +575,7 @@ moe_status moe_expert_ffn(const void* tokens, const int32_t* perm, const int32_t
   if (f16) {
     return run_tc_ffn(tokens, perm, offsets, W1, W2, nullptr, nullptr, T, d, f, E, 0, S_max, S_max,
                       reinterpret_cast<__half*>(ws + kAlign), nullptr, kModeExpertOut, expert_out,
-                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr, status,
-                      /*pdl_first=*/false, s);
+                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, /*pdl_first=*/false, s);
   }
   SimtArgs a;
   memset(&a, 0, sizeof(a));
@@ -669,10 +647,10 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
   const int mode = (k == 1 && !residual) ? kModeDirect : kModeAccum;
   const int S_max = (int)std::min<long long>((long long)T * k, (long long)E * C);
 
-  // status word, the fused router's arrival counter and the split-K counters (one memset)
+  // status word and, next to it, the fused router's arrival counter
   unsigned int* route_counter = reinterpret_cast<unsigned int*>(ws + L.status + sizeof(int));
   MOE_TRY(stage_mark(0, s));
-  MOE_TRY(cudaMemsetAsync(status, 0, L.ctrl_bytes, s));
+  MOE_TRY(cudaMemsetAsync(status, 0, 2 * sizeof(int), s));
   if (f16 && gate_route_small_ok(T, d, E, tokens, Wg)) {
     // decode-sized batch: gate, top-k and dispatch in one launch
     MOE_TRY(launch_gate_route_small(static_cast<const __half*>(tokens), Wg, T, d, E, k, C, logits,
@@ -697,10 +675,7 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
                     residual ? reinterpret_cast<__half*>(ws + L.Hres) : nullptr, mode, out, acc32, r32,
                     slot_w, k == 1 ? slot_of : nullptr,
                     L.partial_bytes ? reinterpret_cast<float*>(ws + L.partial) : nullptr,
-                    L.partial_bytes,
-                    reinterpret_cast<unsigned int*>(ws + L.status + L.split_cnt1),
-                    reinterpret_cast<unsigned int*>(ws + L.status + L.split_cnt2), status,
-                    /*pdl_first=*/true, s);
+                    L.partial_bytes, status, /*pdl_first=*/true, s);
     if (st != MOE_OK) return st;
   } else {
     SimtArgs a;

@@ -118,7 +118,67 @@ __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
   __syncthreads();
 }
 
+// Split-K reduction of the first GEMM: sum the chunks in order, GeLU, round to f16.
+__global__ void splitk_reduce1_kernel(const GemmArgs g, int S_max, int T_res, int f, int f_res) {
+  pdl_wait();
+  pdl_trigger();
+  const int S = g.offsets[g.E];
+  const size_t n = (size_t)(S_max + T_res) * g.part_cols;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += stride) {
+    const int prow = (int)(q / g.part_cols), c = (int)(q % g.part_cols);
+    const bool res = prow >= S_max;
+    const int row = res ? prow - S_max : prow;
+    if (res ? c >= f_res : (c >= f || row >= S)) continue;
+    float v = 0.f;
+    for (int ks = 0; ks < g.ksplit; ++ks) v += g.partial[((size_t)ks * g.part_rows + prow) * g.part_cols + c];
+    const __half h = __float2half_rn(gelu_tanh(v));
+    if (res) g.hres_out[(size_t)row * g.ldhres + c] = h;
+    else g.h_out[(size_t)row * g.ldh + c] = h;
+  }
+}
+
+// Split-K reduction of the second GEMM: sum the chunks in order, then the combine.
+__global__ void splitk_reduce2_kernel(const GemmArgs g, int S_max, int T_res, int d) {
+  pdl_wait();
+  pdl_trigger();
+  const int S = g.offsets[g.E];
+  const size_t n = (size_t)(S_max + T_res) * d;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += stride) {
+    const int prow = (int)(q / d), c = (int)(q % d);
+    const bool res = prow >= S_max;
+    const int row = res ? prow - S_max : prow;
+    if (!res && row >= S) continue;
+    float v = 0.f;
+    for (int ks = 0; ks < g.ksplit; ++ks) v += g.partial[((size_t)ks * g.part_rows + prow) * g.part_cols + c];
+    if (res) {
+      g.r32[(size_t)row * g.ldo + c] = v;
+    } else if (g.mode == kModeExpertOut) {
+      g.out[(size_t)row * g.ldo + c] = __float2half_rn(v);
+    } else {
+      const int tok = g.perm[row];
+      const float w = g.slot_w[row];
+      if (g.mode == kModeDirect) g.out[(size_t)tok * g.ldo + c] = __float2half_rn(w * v);
+      else red_add_f32(g.acc32 + (size_t)tok * g.ldo + c, w * v);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_splitk_reduce1(const GemmArgs& g, int S_max, int T_res, int f, int f_res,
+                                  cudaStream_t s, bool pdl) {
+  const size_t n = (size_t)(S_max + T_res) * g.part_cols;
+  return launch_k(splitk_reduce1_kernel, grid_for(n, 256), 256, 0, s, pdl, g, S_max, T_res, f,
+                  f_res);
+}
+
+cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d, cudaStream_t s,
+                                  bool pdl) {
+  const size_t n = (size_t)(S_max + T_res) * d;
+  return launch_k(splitk_reduce2_kernel, grid_for(n, 256), 256, 0, s, pdl, g, S_max, T_res, d);
+}
 
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s) {
   MOE_LAUNCH(launch_k(zero_f32_kernel, grid_for(n / 4 + 1, 256), 256, 0, s, false, p, n));

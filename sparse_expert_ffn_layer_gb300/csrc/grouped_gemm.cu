@@ -100,20 +100,6 @@ __device__ __forceinline__ Tile decode(int i, const GemmArgs& a, const int32_t* 
   return t;
 }
 
-// Named barrier 1 over the four epilogue warps (threads 64 .. 191).
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-// Same barrier with a vote: true iff every epilogue thread passes true.
-__device__ __forceinline__ bool epi_all(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.and.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
-      : "=r"(r)
-      : "r"(v ? 1u : 0u)
-      : "memory");
-  return r != 0;
-}
-
 template <bool kGatherB, int kEpi, int kMW>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -130,7 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;        // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
-  volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 8);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.misc_off + 16);
   int32_t* soffs = prefix + (a.E + 1);                     // copy of offsets[0 .. E]
   int32_t* row_tok = reinterpret_cast<int32_t*>(smem + L.rows_off);   // [4 warps][nmax]
@@ -347,9 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     int local = 0;
-    // split-K: the four epilogue warps meet at named barrier 1 around each item's fix-up, so
-    // they leave the loop together (the abort decision is a barrier vote, not a flag read)
-    for (int i = blockIdx.x; i < total && (ksplit > 1 || !*abort_flag); i += gridDim.x, ++local) {
+    for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++local) {
       const Tile t = decode(i / ksplit, a, prefix, soffs);
       const int ks = i - (i / ksplit) * ksplit;
       const int buf = local % a.nbuf;
@@ -370,7 +353,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       if (lane == 0) ok = mbar_wait_bounded(&acc_full[buf], use, abort_flag, a.status, a.wait_ns);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (ksplit > 1) ok = epi_all(ok);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
@@ -410,45 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
-      if (ksplit > 1) {
-        // split-K fix-up: the CTA whose chunk of this item arrives last sums every chunk in
-        // chunk order and applies the epilogue (chunks never wait for one another)
-        const int item = i / ksplit;
-        __threadfence();
-        epi_bar();
-        if (threadIdx.x == 64)
-          *fix_flag = atomicAdd(&a.split_cnt[item], 1u) == (unsigned)(ksplit - 1) ? 1 : 0;
-        epi_bar();
-        if (*fix_flag) {
-          __threadfence();
-          const int etid = threadIdx.x - 64;
-          const int cols = mw * kBM;
-          for (int q = etid; q < t.n * cols; q += 128) {
-            const int s = q / cols;
-            const int m = t.mt * cols + (q - s * cols);
-            const int row = t.row0 + s;
-            const int prow = t.res ? a.part_res_row0 + row : row;
-            float v = 0.f;
-            for (int kc = 0; kc < ksplit; ++kc)
-              v += __ldcg(&a.partial[((size_t)kc * a.part_rows + prow) * a.part_cols + m]);
-            if (kEpi == kEpiGeluH) {
-              const __half h = __float2half_rn(gelu_tanh(v));
-              if (t.res) a.hres_out[(size_t)row * a.ldhres + m] = h;
-              else a.h_out[(size_t)row * a.ldh + m] = h;
-            } else if (t.res) {
-              a.r32[(size_t)row * a.ldo + m] = v;
-            } else if (a.mode == kModeExpertOut) {
-              a.out[(size_t)row * a.ldo + m] = __float2half_rn(v);
-            } else {
-              const int tok = a.perm[row];
-              const float w = a.slot_w[row];
-              if (a.mode == kModeDirect) a.out[(size_t)tok * a.ldo + m] = __float2half_rn(w * v);
-              else red_add_f32(a.acc32 + (size_t)tok * a.ldo + m, w * v);
-            }
-          }
-          if (threadIdx.x == 64) a.split_cnt[item] = 0u;     // ready for the next launch
-        }
-      }
     }
   }
 

@@ -88,14 +88,11 @@ struct GemmArgs {
   int drop_d;
   // split-K (decode-sized batches): each tile's K range is cut into ksplit chunks run by
   // different CTAs; chunk ks writes fp32 partial sums to partial[ks][prow][part_cols], where
-  // prow = row (expert slot) or part_res_row0 + token (residual group); the last chunk to
-  // arrive sums the chunks in order and applies the epilogue.  ksplit == 1: epilogue in place.
+  // prow = row (expert slot) or part_res_row0 + token (residual group); a reduce kernel then
+  // sums the chunks in order and applies the epilogue.  ksplit == 1: epilogue in place.
   int ksplit;
   float* partial;
   int part_rows, part_cols, part_res_row0;
-  unsigned int* split_cnt;  // [items] chunks arrived per item, zero at launch; the CTA of the
-                            // last chunk sums the chunks in order, applies the epilogue and
-                            // sets the count back to zero
   // error reporting
   int* status;
   uint64_t wait_ns;
@@ -161,5 +158,11 @@ cudaError_t launch_combine(const void* expert_out, const int32_t* slot_of, const
                            const void* residual_in, int dtype_f16, int T, int d, int k, void* out,
                            cudaStream_t s);
 cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
+// split-K reductions (fixed chunk order): first GEMM -> GeLU -> H / Hres; second GEMM -> the
+// combine of the given mode / r32
+cudaError_t launch_splitk_reduce1(const GemmArgs& g, int S_max, int T_res, int f, int f_res,
+                                  cudaStream_t s, bool pdl = false);
+cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d, cudaStream_t s,
+                                  bool pdl = false);
 
 }  // namespace moe
