@@ -181,6 +181,8 @@ LAYER_CASES = [
     ("moe2p4b_e128_top2", 1, None), ("moe2p4b_e128_top2", 32, 10),
     ("moe2p4b_e128_top2_zipf", 32, 10),
     ("top2_e64", 64, 24), ("top2_e128", 2048, 24),
+    # decode batches whose slots plus residual rows fit the split-K path (residual group split)
+    ("prmoe_e64", 16, None), ("tiny_prmoe_e8", 24, None),
 ]
 
 
