@@ -345,6 +345,28 @@ def test_closed_form_zero_gate_and_zero_tokens(m):
     assert np.all(out0 == 0.0)
 
 
+@pytest.mark.parametrize("k", [1, 2])
+def test_layer_routing_with_tied_gate_columns(m, k):
+    """Experts whose gate columns are identical tie exactly on every token.  The batch is
+    large enough for the tensor-core gate, whose candidates are re-evaluated with the exact
+    chain: the tie must go to the lower index, as in the oracle (top-2: the expert and its
+    duplicate)."""
+    cfg = synth.CONFIGS["moe350m_e128"].at(k=k)
+    T = 256
+    Wg = synth.fill((cfg.d, cfg.E), synth.F32, 7, synth.TID_WG, cfg.w_sigma)
+    Wg[:, 64:] = Wg[:, :64]                        # expert e + 64 duplicates expert e
+    case = Case(cfg, T, seed=7, Wg=Wg)
+    out, idx, slot = case.forward(m)
+    r = case.routing()
+    assert np.array_equal(idx, r.topk_idx) and np.array_equal(slot, r.disp.slot_of)
+    assert np.all(idx[:, 0] < 64)
+    if k == 2:
+        assert np.array_equal(idx[:, 1], idx[:, 0] + 64)
+    rows = sample_rows(r, T, 8)
+    ok, err, bound = within_tol(out[rows], case.reference_rows(rows))
+    assert ok, f"max err {err:.3e} > bound {bound:.3e}"
+
+
 def test_empty_batch_is_a_no_op(m):
     cfg = synth.CONFIGS["moe350m_e128"]
     case = Case(cfg, 4, seed=0)
