@@ -376,8 +376,36 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   g1.part_rows = part_rows;
   g1.part_cols = std::max(f, residual ? f_res : 0);
   g1.part_res_row0 = S_rows;
+  // Larger batches run the residual MLP's first GEMM as a launch of its own: its token rows
+  // are contiguous (16-row boxes instead of row gathers) and its tiles take up to 256 rows,
+  // where the shared launch would re-stream each dense weight block once per 64-row tile.
+  const bool res_apart = residual && ks1 == 1 && T > plan1.nmax;
+  if (res_apart) g1.n_res_rows = 0;
   MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan1.grid, s, pdl && pdl_first));
   if (ks1 > 1) MOE_TRY(launch_splitk_reduce1(g1, S_rows, T_res, f, f_res, s, pdl));
+  if (res_apart) {
+    TcPlan planR;
+    if (!tc_plan(std::min(T, 256), &planR)) return MOE_ERR_CUDA;
+    const long long resR = (T + planR.nmax - 1) / planR.nmax;
+    const int mwR = choose_mw(0, f_res, resR, f_res, planR, 0);
+    CUtensorMap mXr;
+    if (!make_map(&mXr, tokens, d, T, 64, 16)) return MOE_ERR_CUDA;
+    GemmArgs gr;
+    fill_common(gr, planR, /*E=*/0, mwR, status);
+    if (gr.stages < 2) return MOE_ERR_UNSUPPORTED;
+    gr.offsets = offsets;                // no expert group: only offsets[0] (= 0) is read
+    gr.perm = perm;
+    gr.n_res_rows = T;
+    gr.K = d;
+    gr.K_res = d;
+    gr.mt_exp = 1;
+    gr.mt_res = f_res / 128 / mwR;
+    gr.h_out = H;
+    gr.ldh = f;
+    gr.hres_out = Hres;
+    gr.ldhres = f_res;
+    MOE_TRY(launch_grouped_gemm1_rows(mWr1, mXr, mWr1, mXr, gr, planR.grid, s, pdl));
+  }
   MOE_TRY(stage_mark(4, s));
 
   GemmArgs g2;

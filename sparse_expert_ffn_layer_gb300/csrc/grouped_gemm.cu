@@ -463,4 +463,10 @@ cudaError_t launch_grouped_gemm2(const CUtensorMap& A, const CUtensorMap& B, con
   return launch_one<false, kEpiCombine>(A, B, Ar, Br, args, grid, s, pdl);
 }
 
+cudaError_t launch_grouped_gemm1_rows(const CUtensorMap& A, const CUtensorMap& B,
+                                      const CUtensorMap& Ar, const CUtensorMap& Br,
+                                      const GemmArgs& args, int grid, cudaStream_t s, bool pdl) {
+  return launch_one<false, kEpiGeluH>(A, B, Ar, Br, args, grid, s, pdl);
+}
+
 }  // namespace moe

@@ -126,6 +126,12 @@ cudaError_t launch_grouped_gemm1(const CUtensorMap& A, const CUtensorMap& B, con
 cudaError_t launch_grouped_gemm2(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                                  const CUtensorMap& Br, const GemmArgs& args, int grid,
                                  cudaStream_t s, bool pdl = false);
+// The first GEMM's kernel with contiguous token rows (16-row boxes, no gather): the residual
+// MLP's group on its own.
+cudaError_t launch_grouped_gemm1_rows(const CUtensorMap& A, const CUtensorMap& B,
+                                      const CUtensorMap& Ar, const CUtensorMap& Br,
+                                      const GemmArgs& args, int grid, cudaStream_t s,
+                                      bool pdl = false);
 
 // fp32 SIMT path (small layers)
 struct SimtArgs {
