@@ -391,6 +391,10 @@ def run_ours(args):
         for j in range(moe.MOE_STAGE_EVENTS - 1):
             stage_ms[j] += evs[i][j].elapsed_time(evs[i][j + 1])
     stage_ms /= K
+    # spread of single steps (first to last stage event of each staged step; each includes
+    # the event records, so it sits a little above the event-free mean)
+    step_each = np.array([evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)])
+    step_pct = {f"p{q}": float(np.percentile(step_each, q)) for q in (10, 50, 90)}
 
     # end to end through the public API with host buffers: H2D tokens, forward, D2H output
     h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -466,6 +470,7 @@ def run_ours(args):
                            "bytes": layer_bytes, "flops": layer_flops},
         "stage_ms": {name: float(v) for name, v in zip(moe.STAGES, stage_ms)},
         "stage_ms_source": stage_source,
+        "step_ms_staged": step_pct,
         "routing": {"active_experts": A, "kept_slots": S},
         "e2e": {"value": value_e2e, "unit": UNIT, "h2d_bytes_per_step": T * cfg.d * el,
                 "d2h_bytes_per_step": T * cfg.d * el},
