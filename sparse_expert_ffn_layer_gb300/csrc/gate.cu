@@ -11,10 +11,28 @@
 namespace moe {
 namespace {
 
-constexpr int kTT = 64;   // tokens per block tile
+constexpr int kTT = 64;   // tokens per block tile (scalar kernel)
 constexpr int kTE = 64;   // experts per block tile
 constexpr int kKC = 32;   // shared-dimension chunk staged in shared memory
 constexpr int kXP = kKC + 4;  // padded row of the token tile (16-byte aligned rows)
+
+// Token tile of the vector kernel (64, 32 or 16 tokens: 256, 128 or 64 threads): the largest
+// that still gives about 0.8 CTAs per SM, since a batch of a few hundred tokens leaves most SMs
+// idle with 64-token tiles (measured: T = 512 gate 44 -> 32 us with 32-token tiles; T = 4096
+// keeps 64).
+int vec_tile_tokens(int T, int E) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  const long long etiles = (E + kTE - 1) / kTE;
+  for (int t = 64; t > 16; t /= 2)
+    if ((T + t - 1) / t * etiles * 5 >= 4LL * sms) return t;
+  return 16;
+}
 
 template <typename Tin>
 struct XChunk;  // one thread's share of a 64 x 32 token chunk: 8 consecutive values of a row
@@ -51,17 +69,19 @@ struct XChunk<float> {
 // logits[T, E] = x[T, d] . Wg[d, E]; 256 threads, 4 x 4 outputs per thread.  The next chunk
 // is fetched into registers while the current one is multiplied (double-buffered tiles).
 // Vector path: d % 8 == 0 and E % 4 == 0 (16-byte loads); otherwise the scalar kernel below.
-template <typename Tin>
-__global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict__ x,
-                                                          const float* __restrict__ Wg, int T,
-                                                          int d, int E,
-                                                          float* __restrict__ logits) {
+template <typename Tin, int kT>
+__global__ void __launch_bounds__(kT * 4) gate_logits_kernel(const Tin* __restrict__ x,
+                                                            const float* __restrict__ Wg, int T,
+                                                            int d, int E,
+                                                            float* __restrict__ logits) {
   pdl_trigger();   // the top-k kernel may start its launch; it waits for these logits
-  __shared__ __align__(16) float xs[2][kTT][kXP];   // token tile: xs[t][i]
+  constexpr int kThreadsT = kT * 4;                 // 4 x 4 outputs per thread
+  constexpr int kWR = kKC * 16 / kThreadsT;         // Wg rows each thread stages per chunk
+  __shared__ __align__(16) float xs[2][kT][kXP];    // token tile: xs[t][i]
   __shared__ __align__(16) float ws[2][kKC][kTE];   // Wg tile: ws[i][e]
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
-  // loader roles: token row lt, columns lk .. lk+7; Wg rows lw, lw+16 (4 experts at le)
+  const int t0 = blockIdx.x * kT, e0 = blockIdx.y * kTE;
+  // loader roles: token row lt, columns lk .. lk+7; Wg rows lw + q * (threads / 16), 4 experts at le
   const int lt = threadIdx.x >> 2, lk = (threadIdx.x & 3) * 8;
   const int lw = threadIdx.x >> 4, le = (threadIdx.x & 15) * 4;
   float acc[4][4];
@@ -71,7 +91,7 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
 
   XChunk<Tin> xr;
-  float4 wr0, wr1;
+  float4 wr[kWR];
   auto fetch = [&](int k0) {
     const int t = t0 + lt;
     const int kc = min(kKC, d - k0);
@@ -79,16 +99,20 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const Tin* __restrict_
     else xr.zero();
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     const bool eok = e0 + le < E;
-    wr0 = (eok && lw < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw) * E + e0 + le) : z;
-    wr1 = (eok && lw + 16 < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + lw + 16) * E + e0 + le) : z;
+#pragma unroll
+    for (int q = 0; q < kWR; ++q) {
+      const int row = lw + q * (kThreadsT / 16);
+      wr[q] = (eok && row < kc) ? *reinterpret_cast<const float4*>(Wg + (size_t)(k0 + row) * E + e0 + le) : z;
+    }
   };
   auto stash = [&](int buf) {
     float v[8];
     xr.to_f32(v);
     *reinterpret_cast<float4*>(&xs[buf][lt][lk]) = make_float4(v[0], v[1], v[2], v[3]);
     *reinterpret_cast<float4*>(&xs[buf][lt][lk + 4]) = make_float4(v[4], v[5], v[6], v[7]);
-    *reinterpret_cast<float4*>(&ws[buf][lw][le]) = wr0;
-    *reinterpret_cast<float4*>(&ws[buf][lw + 16][le]) = wr1;
+#pragma unroll
+    for (int q = 0; q < kWR; ++q)
+      *reinterpret_cast<float4*>(&ws[buf][lw + q * (kThreadsT / 16)][le]) = wr[q];
   };
 
   fetch(0);
@@ -324,16 +348,36 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
   const bool vec = d % 8 == 0 && E % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(Wg) & 15) == 0 &&
                    (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+  const int vt = vec_tile_tokens(T, E);
+  const dim3 vgrid((T + vt - 1) / vt, (E + kTE - 1) / kTE);
   if (dtype_f16) {
     const __half* xh = static_cast<const __half*>(x);
-    if (vec) MOE_LAUNCH(launch_k(gate_logits_kernel<__half>, grid, 256, 0, s, false, xh, Wg, T, d,
-                                 E, logits));
+    if (vec) {
+      if (vt == 64)
+        MOE_LAUNCH(launch_k(gate_logits_kernel<__half, 64>, vgrid, 256, 0, s, false, xh, Wg, T, d,
+                            E, logits));
+      else if (vt == 32)
+        MOE_LAUNCH(launch_k(gate_logits_kernel<__half, 32>, vgrid, 128, 0, s, false, xh, Wg, T, d,
+                            E, logits));
+      else
+        MOE_LAUNCH(launch_k(gate_logits_kernel<__half, 16>, vgrid, 64, 0, s, false, xh, Wg, T, d,
+                            E, logits));
+    }
     else MOE_LAUNCH(launch_k(gate_logits_scalar_kernel<__half>, grid, 256, 0, s, false, xh, Wg, T,
                              d, E, logits));
   } else {
     const float* xf = static_cast<const float*>(x);
-    if (vec) MOE_LAUNCH(launch_k(gate_logits_kernel<float>, grid, 256, 0, s, false, xf, Wg, T, d, E,
-                                 logits));
+    if (vec) {
+      if (vt == 64)
+        MOE_LAUNCH(launch_k(gate_logits_kernel<float, 64>, vgrid, 256, 0, s, false, xf, Wg, T, d,
+                            E, logits));
+      else if (vt == 32)
+        MOE_LAUNCH(launch_k(gate_logits_kernel<float, 32>, vgrid, 128, 0, s, false, xf, Wg, T, d,
+                            E, logits));
+      else
+        MOE_LAUNCH(launch_k(gate_logits_kernel<float, 16>, vgrid, 64, 0, s, false, xf, Wg, T, d,
+                            E, logits));
+    }
     else MOE_LAUNCH(launch_k(gate_logits_scalar_kernel<float>, grid, 256, 0, s, false, xf, Wg, T, d,
                              E, logits));
   }
