@@ -20,17 +20,21 @@ constexpr int kXP = kKC + 4;  // padded row of the token tile (16-byte aligned r
 // that still gives about 0.8 CTAs per SM, since a batch of a few hundred tokens leaves most SMs
 // idle with 64-token tiles (measured: T = 512 gate 44 -> 32 us with 32-token tiles; T = 4096
 // keeps 64).
-int vec_tile_tokens(int T, int E) {
+int sm_count() {
   static int sms = 0;
   if (sms == 0) {
-    int dev = 0;
+    int dev = 0, n = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    sms = n > 0 ? n : 1;
   }
+  return sms;
+}
+
+int vec_tile_tokens(int T, int E) {
   const long long etiles = (E + kTE - 1) / kTE;
   for (int t = 64; t > 16; t /= 2)
-    if ((T + t - 1) / t * etiles * 5 >= 4LL * sms) return t;
+    if ((T + t - 1) / t * etiles * 5 >= 4LL * sm_count()) return t;
   return 16;
 }
 
@@ -218,12 +222,13 @@ __global__ void __launch_bounds__(256) gate_logits_scalar_kernel(const Tin* __re
 }
 
 // ---------------------------------------------------------------------------------------
-// Small batches (T <= 64): one thread per (token, expert) chain.  Block = 8 tokens (warps) x
-// 32 experts (lanes); raw Wg and token chunks stream through a four-deep cp.async ring, so
-// the cost is close to the d dependent multiply-adds of one chain instead of a 64-token tile.
+// Small and medium batches: one thread per expert and M tokens (M independent chains).
+// Block = 8 warps x M tokens x 32 experts (lanes); raw Wg and token chunks stream through a
+// four-deep cp.async ring, so with few tokens the cost is close to the d dependent
+// multiply-adds of one chain instead of a 64-token tile's.
 constexpr int kSKC = 64;       // shared-dimension chunk
 constexpr int kSStages = 4;    // ring depth
-constexpr int kSTok = 8;       // tokens per block (one per warp)
+constexpr int kSWarps = 8;     // warps per block; each owns M consecutive tokens
 constexpr int kSExp = 32;      // experts per block (one per lane)
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
@@ -237,23 +242,41 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <typename Tin>
+template <typename Tin, int M>
 __host__ __device__ constexpr size_t small_slot_bytes() {
-  return (size_t)kSKC * kSExp * sizeof(float) + (size_t)kSTok * kSKC * sizeof(Tin);
+  return (size_t)kSKC * kSExp * sizeof(float) + (size_t)kSWarps * M * kSKC * sizeof(Tin);
 }
 
-// Needs d % 64 == 0, E % 4 == 0, 16-byte aligned rows.
-template <typename Tin>
+// Eight 16-byte row pieces of a staged token chunk, widened to fp32 (exact).
+__device__ __forceinline__ void unpack16(const uint4& u, float* f, const float*) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& u, float* f, const __half*) {
+  const uint32_t r[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&r[q]));
+    f[2 * q] = v.x;
+    f[2 * q + 1] = v.y;
+  }
+}
+
+// Needs d % 64 == 0, E % 4 == 0, 16-byte aligned rows.  Warp w owns tokens t0 + w*M .. +M-1,
+// lane l expert e0 + l: M independent chains per thread, each in ascending i.
+template <typename Tin, int M>
 __global__ void __launch_bounds__(256) gate_logits_small_kernel(const Tin* __restrict__ x,
                                                                 const float* __restrict__ Wg,
                                                                 int T, int d, int E,
                                                                 float* __restrict__ logits) {
   pdl_trigger();   // the top-k kernel may start its launch; it waits for these logits
   extern __shared__ __align__(16) uint8_t ssm[];
+  constexpr int kTok = kSWarps * M;
+  constexpr int kPer = 16 / (int)sizeof(Tin);   // values per 16-byte piece
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int e0 = blockIdx.x * kSExp, t0 = blockIdx.y * kSTok;
+  const int e0 = blockIdx.x * kSExp, t0 = blockIdx.y * kTok;
   const int nch = d / kSKC;
-  constexpr size_t slot = small_slot_bytes<Tin>();
+  constexpr size_t slot = small_slot_bytes<Tin, M>();
   auto issue = [&](int c) {
     uint8_t* base = ssm + (size_t)(c % kSStages) * slot;
     const int k0 = c * kSKC;
@@ -264,10 +287,9 @@ __global__ void __launch_bounds__(256) gate_logits_small_kernel(const Tin* __res
       cp_async16(base + (row * kSExp + col) * 4, Wg + (size_t)(k0 + row) * E + min(e, E - 4),
                  e < E ? 16 : 0);
     }
-    // tokens t0 .. t0+7, columns k0 .. k0+63
-    constexpr int kPer = 16 / (int)sizeof(Tin);
+    // tokens t0 .. t0+kTok-1, columns k0 .. k0+63
     uint8_t* xb = base + (size_t)kSKC * kSExp * 4;
-    for (int q = threadIdx.x; q < kSTok * (kSKC / kPer); q += 256) {
+    for (int q = threadIdx.x; q < kTok * (kSKC / kPer); q += 256) {
       const int tt = q / (kSKC / kPer), col = (q % (kSKC / kPer)) * kPer;
       const int t = t0 + tt;
       cp_async16(xb + (tt * kSKC + col) * sizeof(Tin), x + (size_t)min(t, T - 1) * d + k0 + col,
@@ -279,7 +301,9 @@ __global__ void __launch_bounds__(256) gate_logits_small_kernel(const Tin* __res
     if (c < nch) issue(c);
     cp_async_commit();
   }
-  float acc = 0.0f;
+  float acc[M];
+#pragma unroll
+  for (int j = 0; j < M; ++j) acc[j] = 0.0f;
   for (int c = 0; c < nch; ++c) {
     if (c + kSStages - 1 < nch) issue(c + kSStages - 1);
     cp_async_commit();
@@ -287,15 +311,58 @@ __global__ void __launch_bounds__(256) gate_logits_small_kernel(const Tin* __res
     __syncthreads();
     const uint8_t* base = ssm + (size_t)(c % kSStages) * slot;
     const float* ws = reinterpret_cast<const float*>(base);
-    const Tin* xs = reinterpret_cast<const Tin*>(base + (size_t)kSKC * kSExp * 4) + w * kSKC;
-#pragma unroll 16
-    for (int kk = 0; kk < kSKC; ++kk)            // ascending i
-      acc = __fmaf_rn(to_f32<Tin>(xs[kk]), ws[kk * kSExp + lane], acc);
+    const Tin* xs = reinterpret_cast<const Tin*>(base + (size_t)kSKC * kSExp * 4) + w * M * kSKC;
+#pragma unroll 2
+    for (int kk = 0; kk < kSKC; kk += kPer) {
+      float xv[M][kPer];
+#pragma unroll
+      for (int j = 0; j < M; ++j)
+        unpack16(*reinterpret_cast<const uint4*>(xs + j * kSKC + kk), xv[j], xs);
+#pragma unroll
+      for (int v = 0; v < kPer; ++v) {             // ascending i
+        const float wv = ws[(kk + v) * kSExp + lane];
+#pragma unroll
+        for (int j = 0; j < M; ++j) acc[j] = __fmaf_rn(xv[j][v], wv, acc[j]);
+      }
+    }
     __syncthreads();                             // the slot may be refilled next
   }
   cp_async_wait<0>();
-  const int t = t0 + w, e = e0 + lane;
-  if (t < T && e < E) logits[(size_t)t * E + e] = acc;
+  const int e = e0 + lane;
+#pragma unroll
+  for (int j = 0; j < M; ++j) {
+    const int t = t0 + w * M + j;
+    if (t < T && e < E) logits[(size_t)t * E + e] = acc[j];
+  }
+}
+
+// Tokens per warp of the small-batch kernel, 0 where the tiled kernel is used instead: one
+// token per warp while that fits one wave of CTAs, two while it fits two waves, else the
+// 4x4-per-thread tiled kernel, whose fewer shared-memory reads per multiply-add win once every
+// SM is busy.  Measured gate times (350M+MoE-128 layer, d 1024, E 128; tiled -> this kernel):
+// T 128 34 -> 17 us, T 512 34 -> 19 us, T 1024 34 -> 26 us; T 2048 keeps the tiled kernel
+// (33 us against 42 with two tokens per warp).  PR-MoE E 64 (d 2048): T 256 60 -> 26 us,
+// T 2048 61 -> 44 us.
+int small_tokens_per_warp(int T, int E) {
+  const long long etiles = (E + kSExp - 1) / kSExp, sms = sm_count();
+  if (T <= 64 || etiles * ((T + kSWarps - 1) / kSWarps) <= sms) return 1;
+  if (etiles * ((T + 2 * kSWarps - 1) / (2 * kSWarps)) <= 2 * sms) return 2;
+  return 0;
+}
+
+template <typename Tin>
+cudaError_t launch_small(const Tin* x, const float* Wg, int T, int d, int E, float* logits,
+                         int m, cudaStream_t s) {
+  auto go = [&](auto kern, int M, size_t smem) -> cudaError_t {
+    const dim3 g((E + kSExp - 1) / kSExp, (T + kSWarps * M - 1) / (kSWarps * M));
+    return launch_k(kern, g, 256, smem, s, false, x, Wg, T, d, E, logits);
+  };
+  if constexpr (sizeof(Tin) == 2) {  // 48 KB ring; fp32 rows would need more than the default
+    if (m == 4)
+      return go(gate_logits_small_kernel<Tin, 4>, 4, kSStages * small_slot_bytes<Tin, 4>());
+  }
+  if (m >= 2) return go(gate_logits_small_kernel<Tin, 2>, 2, kSStages * small_slot_bytes<Tin, 2>());
+  return go(gate_logits_small_kernel<Tin, 1>, 1, kSStages * small_slot_bytes<Tin, 1>());
 }
 
 struct PlainLoad {
@@ -331,17 +398,12 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
                                float* logits, cudaStream_t s) {
   const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
                        (reinterpret_cast<uintptr_t>(Wg) & 15) == 0;
-  if (T <= 64 && d % kSKC == 0 && E % 4 == 0 && aligned) {
-    dim3 g((E + kSExp - 1) / kSExp, (T + kSTok - 1) / kSTok);
-    if (dtype_f16) {
-      const size_t smem = kSStages * small_slot_bytes<__half>();
-      MOE_LAUNCH(launch_k(gate_logits_small_kernel<__half>, g, 256, smem, s, false,
-                          static_cast<const __half*>(x), Wg, T, d, E, logits));
-    } else {
-      const size_t smem = kSStages * small_slot_bytes<float>();
-      MOE_LAUNCH(launch_k(gate_logits_small_kernel<float>, g, 256, smem, s, false,
-                          static_cast<const float*>(x), Wg, T, d, E, logits));
-    }
+  const int m = small_tokens_per_warp(T, E);
+  if (m > 0 && d % kSKC == 0 && E % 4 == 0 && aligned) {
+    if (dtype_f16)
+      MOE_LAUNCH(launch_small(static_cast<const __half*>(x), Wg, T, d, E, logits, m, s));
+    else
+      MOE_LAUNCH(launch_small(static_cast<const float*>(x), Wg, T, d, E, logits, m, s));
     return cudaGetLastError();
   }
   dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);

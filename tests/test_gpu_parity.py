@@ -36,7 +36,9 @@ def _gate(m, tokens, Wg, k, logits_in=None):
 # ------------------------------------------------------------------------------ gate
 @pytest.mark.parametrize("name,T", [("tiny_fp32", 128), ("moe350m_e128", 1), ("moe350m_e128", 777),
                                     ("moe1p3b_e128_zipf", 256), ("moe2p4b_e128_top2", 1024),
-                                    ("moe2p4b_e128_top2_zipf", 333)])
+                                    ("moe2p4b_e128_top2_zipf", 333), ("moe350m_e128", 2000),
+                                    ("moe350m_e128", 4100), ("prmoe_e64", 1500),
+                                    ("prmoe_e64", 2500)])
 def test_gate_bit_exact(m, name, T):
     cfg = synth.CONFIGS[name]
     inp = synth.host_inputs(cfg, T, seed=3, with_experts=False)
