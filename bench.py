@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -182,7 +183,22 @@ class OracleRunner:
                 f"a full oracle layer call (own routing and capacity), host weights drawn untimed")
 
 
+def cpu_model():
+    """The host CPU's name as the kernel reports it (model name, else the Arm part number)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        info = []
+    for key in ("model name", "Model name", "CPU part"):
+        for line in info:
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip() + ("" if key != "CPU part" else
+                                                        f" (CPU part, {platform.machine()})")
+    return platform.machine()
+
+
 def oracle_tokens_per_s(cfg, T, seed, budget_s):
+    """The oracle on all host cores (about 3/4 of the budget), then on one core (the rest)."""
     r = OracleRunner(cfg, T, seed)
     n = r.size_for(budget_s / 4)
     spent, done, steps = 0.0, 0, 0
@@ -190,7 +206,16 @@ def oracle_tokens_per_s(cfg, T, seed, budget_s):
         spent += r.run(n)
         done += n
         steps += 1
-    return done / spent, r.oracle.num_threads(), r.describe(n, steps) + f", {spent:.1f} s"
+    cores = r.oracle.num_threads()
+    r.oracle.set_num_threads(1)
+    try:
+        n1 = r.size_for(budget_s / 8)
+        one = r.run(n1)
+    finally:
+        r.oracle.set_num_threads(cores)
+    extra = {"single_core_value": n1 / one, "single_core_sample": f"{n1} tokens, {one:.1f} s",
+             "nproc": os.cpu_count(), "cpu_model": cpu_model()}
+    return done / spent, cores, r.describe(n, steps) + f", {spent:.1f} s", extra
 
 
 def run_reference(args):
@@ -373,6 +398,23 @@ def run_ours(args):
         raise RuntimeError(f"device status {moe.moe_status_string(status)}")
     ms = e0.elapsed_time(e1)
 
+    # decode sizes: the same steps with warm weights (one batch's graph replayed, so its
+    # routed experts' weights stay in L2 from one step to the next), beside the cold number
+    warm = None
+    if plain and T <= 64 and world == 1:
+        for _ in range(3):
+            plain[0].replay()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        for _ in range(K):
+            plain[0].replay()
+        w1.record(stream)
+        torch.cuda.synchronize()
+        wms = w0.elapsed_time(w1)
+        warm = {"value": job_tokens_per_s(1, T, K, wms), "unit": UNIT, "ms_per_step": wms / K,
+                "active_experts": stats[0][0],
+                "mode": "one token batch replayed K times: its routed experts' weights stay in L2"}
+
     # stage pass: the same K steps, each with its own stage events
     if args.no_graph:
         for i in range(K):
@@ -510,10 +552,12 @@ def run_ours(args):
         "launch": "direct" if args.no_graph else "one CUDA graph per step, replayed back to back",
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
+    if warm is not None:
+        line["warm_l2"] = warm
     if world == 1 and not args.no_cpu_baseline:
-        rate, cores, desc = oracle_tokens_per_s(cfg, T, seed, args.cpu_budget_s)
+        rate, cores, desc, extra = oracle_tokens_per_s(cfg, T, seed, args.cpu_budget_s)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": desc}
+                                "sample": desc, **extra}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

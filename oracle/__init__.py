@@ -60,6 +60,8 @@ def lib():
         L.oracle_combine_rows.restype = _I
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = _I
+        L.oracle_set_num_threads.argtypes = [_I]
+        L.oracle_set_num_threads.restype = None
         _lib = L
     return _lib
 
@@ -87,6 +89,11 @@ def gelu(x: float) -> float:
 
 def num_threads() -> int:
     return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of later oracle calls (OpenMP); results do not depend on it."""
+    lib().oracle_set_num_threads(int(n))
 
 
 def gate_logits(x: np.ndarray, Wg: np.ndarray) -> np.ndarray:

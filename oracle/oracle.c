@@ -304,3 +304,12 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Thread count of later calls (timing of the oracle on one core and on all cores). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
