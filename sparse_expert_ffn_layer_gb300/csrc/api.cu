@@ -1,6 +1,7 @@
 // C-ABI front end (include/moe.h): argument checks, workspace carving, TMA descriptors and the
 // launch sequence of each entry point.  All device work is in the kernels of this library.
 #include <math.h>
+#include <cmath>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -231,6 +232,29 @@ int choose_mw(long long row_tiles, int M_exp, long long res_tiles, int M_res, co
   return 1;
 }
 
+// Second GEMM: a correction of choose_mw from the row tiles a batch is expected to have
+// (the experts that S_rows uniform draws hit, plus tiles for rows beyond one tile each).
+// Items of four weight blocks win where they come to 1.5-2 waves (350M+MoE-128 layer:
+// T = 512 356.5 -> 338.5 us, T = 4096 407.9 -> 406.2 us per step), not at about one wave
+// (T = 128: 258 -> 279 us); where four blocks do not fit TMEM, two beat one from 3.5 waves
+// on (PR-MoE E 64 at T = 2048: 993 -> 957 us).  Elsewhere choose_mw's pick stands.
+int choose_mw2(int S_rows, int M, long long res_tiles, const TcPlan& p, int E, int picked) {
+  auto fits = [&](int mw) {
+    return M % (128 * mw) == 0 && nbuf_for(mw, p.acc_cols) > 0 &&
+           gemm_stages_for(p.nmax, E, mw, p.smem_optin) >= 3;
+  };
+  const double hit = E * (1.0 - std::pow(1.0 - 1.0 / E, (double)S_rows));
+  const double tiles = std::min<double>(hit, S_rows) +
+                       std::max(0.0, S_rows - hit * p.nmax) / p.nmax + (double)res_tiles;
+  auto waves = [&](int mw) { return tiles * (M / (128 * mw)) / p.grid; };
+  if (fits(4)) {
+    if (waves(4) >= 1.5 && waves(4) <= 2.0) return 4;
+  } else if (picked == 1 && fits(2) && waves(2) >= 3.5) {
+    return 2;
+  }
+  return picked;
+}
+
 // Decode-sized batches: weight blocks per item (mw) and K chunks per item (ks) together.
 // All work units (items x chunks) should run in one round, one per CTA; the widest mw that
 // still spreads the weights over at least half the SMs wins (measured: wider items keep more
@@ -322,7 +346,7 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   const long long tiles2 = std::min(E, S_rows) + S_rows / plan2.nmax;
   const long long res2 = residual ? (T + plan2.nmax - 1) / plan2.nmax : 0;
   int mw1 = choose_mw(tiles1, f, res1, f_res, plan1, E);
-  int mw2 = choose_mw(tiles2, d, res2, d, plan2, E);
+  int mw2 = choose_mw2(S_rows, d, res2, plan2, E, choose_mw(tiles2, d, res2, d, plan2, E));
   int ks1 = 1, ks2 = 1;
   if (partial) {
     choose_split(tiles1, f, res1, f_res, d / 64, plan1, E, &mw1, &ks1);
