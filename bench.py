@@ -264,14 +264,18 @@ def job_tokens_per_s(world, T, K, ms):
 
 # ------------------------------------------------------------------------ GPU arm
 def traffic_record(kernel_file):
-    """Per-launch DRAM bytes from the committed ncu summary, if taken on this kernel source."""
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on this kernel source and
+    this launch plan (the plan file chooses the kernel variant and its tiles)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
-    src = open(kernel_file, "rb").read()
-    if rec.get("kernel_sha256") != hashlib.sha256(src).hexdigest():
-        return None
+    for key_file, key_sha in ((kernel_file, "kernel_sha256"),
+                              (os.path.join(ROOT, rec.get("plan_file", "")), "plan_sha256")):
+        if not os.path.isfile(key_file):
+            return None
+        if rec.get(key_sha) != hashlib.sha256(open(key_file, "rb").read()).hexdigest():
+            return None
     return rec
 
 
