@@ -237,7 +237,9 @@ int choose_mw(long long row_tiles, int M_exp, long long res_tiles, int M_res, co
 // Items of four weight blocks win where they come to 1.5-2 waves (350M+MoE-128 layer:
 // T = 512 356.5 -> 338.5 us, T = 4096 407.9 -> 406.2 us per step), not at about one wave
 // (T = 128: 258 -> 279 us); where four blocks do not fit TMEM, two beat one from 3.5 waves
-// on (PR-MoE E 64 at T = 2048: 993 -> 957 us).  Elsewhere choose_mw's pick stands.
+// on (PR-MoE E 64 at T = 2048: 993 -> 957 us); and two instead of four where four leave the
+// last wave under 90 % full and two fill it at least 10 points better (1.3B+MoE-128 layer,
+// Zipf(1.1), T = 8192: 1456 -> 1412 us).  Elsewhere choose_mw's pick stands.
 int choose_mw2(int S_rows, int M, long long res_tiles, const TcPlan& p, int E, int picked) {
   auto fits = [&](int mw) {
     return M % (128 * mw) == 0 && nbuf_for(mw, p.acc_cols) > 0 &&
@@ -247,8 +249,11 @@ int choose_mw2(int S_rows, int M, long long res_tiles, const TcPlan& p, int E, i
   const double tiles = std::min<double>(hit, S_rows) +
                        std::max(0.0, S_rows - hit * p.nmax) / p.nmax + (double)res_tiles;
   auto waves = [&](int mw) { return tiles * (M / (128 * mw)) / p.grid; };
+  // share of the CTA slots of the last, partly filled wave that have work
+  auto fill = [&](int mw) { const double w = waves(mw); return w / std::ceil(w); };
   if (fits(4)) {
     if (waves(4) >= 1.5 && waves(4) <= 2.0) return 4;
+    if (picked == 4 && fits(2) && fill(4) < 0.9 && fill(2) >= fill(4) + 0.1) return 2;
   } else if (picked == 1 && fits(2) && waves(2) >= 3.5) {
     return 2;
   }
