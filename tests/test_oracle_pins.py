@@ -475,3 +475,30 @@ def test_golden_tiny_fp32(oracle_mod):
     assert [float.fromhex(v) for v in data["logits_row0"]] == r.logits[0].astype(np.float64).tolist()
     ref = np.array([float(v) for v in data["out_rows_0_1_127"]]).reshape(3, -1)
     assert np.allclose(out[[0, 1, 127]], ref, rtol=1e-13, atol=1e-17)
+
+
+# ---------------------------------------------------------------- thread count
+def test_layer_independent_of_thread_count(oracle_mod):
+    """The oracle's results do not depend on how many host threads run it (each token's
+    chain and FFN run in one thread, in a fixed order), so the one-core and all-core timings
+    of the CPU baseline time the same computation."""
+    rng = np.random.default_rng(11)
+    T, d, f, E, cf = 40, 32, 64, 8, 1.25
+    x = rng.standard_normal((T, d)).astype(np.float16)
+    Wg = (rng.standard_normal((d, E)) * 0.3).astype(np.float32)
+    W1 = (rng.standard_normal((E, d, f)) * 0.2).astype(np.float16)
+    W2 = (rng.standard_normal((E, f, d)) * 0.2).astype(np.float16)
+    Wr1 = (rng.standard_normal((d, 48)) * 0.2).astype(np.float16)
+    Wr2 = (rng.standard_normal((48, d)) * 0.2).astype(np.float16)
+    threads = oracle_mod.num_threads()
+    try:
+        oracle_mod.set_num_threads(1)
+        assert oracle_mod.num_threads() == 1
+        one, r1 = oracle_mod.layer_forward(x, Wg, W1, W2, 2, cf, Wr1, Wr2)
+    finally:
+        oracle_mod.set_num_threads(threads)
+    assert oracle_mod.num_threads() == threads
+    many, rn = oracle_mod.layer_forward(x, Wg, W1, W2, 2, cf, Wr1, Wr2)
+    assert np.array_equal(r1.logits.view(np.uint32), rn.logits.view(np.uint32))
+    assert np.array_equal(r1.disp.slot_of, rn.disp.slot_of)
+    assert np.array_equal(one.view(np.uint64), many.view(np.uint64))
