@@ -65,7 +65,10 @@ typedef enum {
   MOE_ERR_WORKSPACE = 3,      /* workspace missing or smaller than moe_workspace_size */
   MOE_ERR_CUDA = 4,           /* a CUDA launch or API call failed */
   MOE_ERR_TIMEOUT = 5,        /* device side: a bounded wait gave up (status word) */
-  MOE_ERR_DEVICE_BOUNDS = 6   /* device side: an index failed its bounds check (status word) */
+  MOE_ERR_DEVICE_BOUNDS = 6   /* device side: an index failed its bounds check (status word);
+                                 reserved: no kernel of this build raises it, and perm /
+                                 offsets / slot_of given to moe_expert_ffn / moe_combine must
+                                 be as moe_dispatch writes them */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_F16 = 1 } moe_dtype;           /* activations and expert weights */
