@@ -47,6 +47,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -55,6 +56,17 @@
 
 #define OR_F32 0
 #define OR_F16 1
+
+/* malloc that stops the process when the host is out of memory (a checker that went on
+ * with a null buffer would report garbage as a reference). */
+static void* xmalloc(size_t bytes) {
+  void* p = malloc(bytes ? bytes : 1);
+  if (!p) {
+    fprintf(stderr, "oracle: out of host memory (%zu bytes)\n", bytes);
+    abort();
+  }
+  return p;
+}
 
 /* IEEE binary16 bit pattern -> double, from the format's definition. */
 double oracle_half_to_double(uint16_t h) {
@@ -92,7 +104,7 @@ void oracle_gate_logits(const void* x, int x_dtype, const float* Wg, int T, int 
 /* Step 2: softmax over E (double) and top-k selection on the logits. */
 void oracle_softmax_topk(const float* logits, int T, int E, int k, double* probs /* nullable */,
                          int32_t* topk_idx, double* topk_w) {
-  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  double* p = (double*)xmalloc(sizeof(double) * (size_t)E);
   for (int t = 0; t < T; ++t) {
     const float* l = logits + (size_t)t * E;
     int e1 = 0;
@@ -146,7 +158,7 @@ int oracle_capacity(int T, int E, double cf) {
  */
 int oracle_dispatch(const int32_t* topk_idx, int T, int E, int k, int C, int32_t* counts_raw,
                     int32_t* kept, int32_t* offsets, int32_t* perm, int32_t* slot_of) {
-  int32_t* rank = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
+  int32_t* rank = (int32_t*)xmalloc(sizeof(int32_t) * (size_t)T * k);
   for (int e = 0; e < E; ++e) counts_raw[e] = 0;
   for (int t = 0; t < T; ++t)
     for (int j = 0; j < k; ++j) {
@@ -188,7 +200,7 @@ int oracle_dispatch(const int32_t* topk_idx, int T, int E, int k, int C, int32_t
 int oracle_dispatch_shard(const int32_t* topk_idx, int T, int E, int k, int C,
                           const int32_t* base, int32_t* counts_raw, int32_t* kept,
                           int32_t* offsets, int32_t* perm, int32_t* slot_of) {
-  int32_t* rank = (int32_t*)malloc(sizeof(int32_t) * ((size_t)T * k + 1));
+  int32_t* rank = (int32_t*)xmalloc(sizeof(int32_t) * ((size_t)T * k + 1));
   for (int e = 0; e < E; ++e) counts_raw[e] = 0;
   for (int t = 0; t < T; ++t)
     for (int j = 0; j < k; ++j) {
@@ -245,7 +257,7 @@ static void mlp_token(const void* x, int x_dtype, size_t x_off, const void* W_in
 
 void oracle_expert_ffn(const void* x_row, int x_dtype, const void* W1e, const void* W2e,
                        int w_dtype, int d, int f, double* y) {
-  double* h = (double*)malloc(sizeof(double) * (size_t)f);
+  double* h = (double*)xmalloc(sizeof(double) * (size_t)f);
   mlp_token(x_row, x_dtype, 0, W1e, W2e, w_dtype, d, f, h, y);
   free(h);
 }
@@ -266,8 +278,8 @@ int oracle_combine_rows(const void* x, int x_dtype, int T, int d, int f, int k,
   int fmax = f > f_res ? f : f_res;
 #pragma omp parallel
   {
-    double* h = (double*)malloc(sizeof(double) * (size_t)(fmax > 0 ? fmax : 1));
-    double* y = (double*)malloc(sizeof(double) * (size_t)d);
+    double* h = (double*)xmalloc(sizeof(double) * (size_t)(fmax > 0 ? fmax : 1));
+    double* y = (double*)xmalloc(sizeof(double) * (size_t)d);
 #pragma omp for schedule(dynamic, 1)
     for (int r = 0; r < n_rows; ++r) {
       int t = rows ? rows[r] : r;

@@ -422,6 +422,39 @@ def test_single_expert_reduces_to_mlp(oracle_mod):
     assert np.allclose(out, ref, rtol=1e-12, atol=1e-13)
 
 
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+def test_expert_ffn_single_row(oracle_mod, dtype):
+    """The one-row expert FFN (the reference of the standalone expert-FFN checks) against
+    torch float64 (library matmuls and torch's own tanh GeLU), with d != f so that a swapped
+    or transposed W1 / W2 cannot pass; then the same row through the one-expert, weight-1
+    combine, and the output's linearity in W2."""
+    import torch
+    rng = np.random.default_rng(21)
+    d, f = 24, 56
+    W1 = (rng.standard_normal((d, f)) * 0.3).astype(dtype)
+    W2 = (rng.standard_normal((f, d)) * 0.3).astype(dtype)
+    xs = rng.standard_normal((5, d)).astype(dtype)
+    for x in xs:
+        y = oracle_mod.expert_ffn(x, W1, W2)
+        assert y.shape == (d,) and y.dtype == np.float64
+        xt = torch.tensor(x.astype(np.float64))[None, :]
+        h = torch.nn.functional.gelu(xt @ torch.tensor(W1.astype(np.float64)), approximate="tanh")
+        ref = (h @ torch.tensor(W2.astype(np.float64))).numpy()[0]
+        assert np.allclose(y, ref, rtol=1e-12, atol=1e-14)
+        # a scaled W2 scales the output (exact: powers of two)
+        y4 = oracle_mod.expert_ffn(x, W1, (W2.astype(np.float64) * 4).astype(dtype))
+        assert np.array_equal(y4, 4 * y)
+    assert np.all(oracle_mod.expert_ffn(np.zeros(d, dtype), W1, W2) == 0.0)
+    # the same rows through the layer's combine with one expert and weight 1
+    T = xs.shape[0]
+    r = oracle_mod.Routing(logits=np.zeros((T, 1), np.float32), probs=np.ones((T, 1)),
+                           topk_idx=np.zeros((T, 1), np.int32), topk_w=np.ones((T, 1)),
+                           disp=oracle_mod.dispatch(np.zeros((T, 1), np.int32), 1, T))
+    out = oracle_mod.combine_rows(xs, r, W1[None], W2[None])
+    for t in range(T):
+        assert np.array_equal(out[t], oracle_mod.expert_ffn(xs[t], W1, W2))
+
+
 def test_stack_of_single_expert_layers_is_an_mlp_chain(oracle_mod):
     """A stack of E = 1 layers (one with a residual MLP) is the plain chain of MLPs, with each
     layer's output rounded to fp16 before the next layer; checked against torch float64."""
