@@ -1,12 +1,13 @@
 #!/usr/bin/env python3
 """Benchmark of the MoE FFN layer forward on GB300: tokens/s and fraction of roofline.
 
-Default workload: the 350M+MoE-128 layer (d=1024, f=4096, E=128 experts, top-1, capacity
-factor 1.25) at T = 4096 tokens, fp16 weights and activations with fp32 accumulation, all
-expert weights (2.15 GB) resident in HBM.  A step is one moe_layer_forward call (gate,
+Default workload: the 2.4B+MoE-128 layer (d=3584, f=14336, E=128 experts, top-2 with
+normalised gate weights, capacity factor 1.25, uniform routing) at T = 16384 tokens, fp16
+weights and activations with fp32 accumulation, all expert weights (26.3 GB) resident in HBM:
+the largest configured layer that one GPU holds.  A step is one moe_layer_forward call (gate,
 dispatch, both expert GEMMs with fused GeLU and combine) on one of 4 seeded token batches,
 cycled so routing changes from step to step; the expert weights alone exceed L2 (129 MB)
-several times over, so every step streams them from HBM.
+two hundred times over, so every step streams them from HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -42,11 +43,11 @@ UNIT = "tokens/s"
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="moe350m_e128")
-    p.add_argument("--tokens", type=int, default=4096)
+    p.add_argument("--workload", default="moe2p4b_e128_top2")
+    p.add_argument("--tokens", type=int, default=16384)
     p.add_argument("--experts", type=int, default=None,
                    help="override the workload's expert count (smaller profiling cases)")
     p.add_argument("--stack", default=None,
@@ -70,6 +71,22 @@ def bench_config(args):
     if getattr(args, "capacity_factor", None) is not None:
         cfg = cfg.at(cf=args.capacity_factor)
     return cfg, T
+
+
+MODEL_NAMES = {
+    "moe350m_e128": "350M+MoE-128 layer, top-1",
+    "moe1p3b_e128_zipf": "1.3B+MoE-128 layer, top-1, Zipf(1.1) routing",
+    "prmoe_e64": "PR-MoE residual layer, E 64", "prmoe_e128": "PR-MoE residual layer, E 128",
+    "top2_e64": "Top2-MoE at the PR-MoE shape, E 64", "top2_e128": "Top2-MoE at the PR-MoE shape, E 128",
+    "moe2p4b_e128_top2": "2.4B+MoE-128 layer, top-2, uniform routing",
+    "moe2p4b_e128_top2_zipf": "2.4B+MoE-128 layer, top-2, Zipf(1.2) routing",
+}
+
+
+def workload_name(cfg):
+    """The workload as the JSON line names it: registry key and the model layer it is."""
+    what = MODEL_NAMES.get(cfg.name)
+    return f"{cfg.name}: {what}" if what else cfg.name
 
 
 def cf_json(cf):
@@ -239,8 +256,8 @@ def run_reference(args):
         "steps": K, "warmup": W, "ms_per_step": 1000.0 * elapsed / max(1, K),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": cfg.name, "T": T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
-                   "capacity_factor": cf_json(cfg.cf)},
+        "config": {"workload": workload_name(cfg), "T": T, "d": cfg.d, "f": cfg.f, "E": cfg.E,
+                   "k": cfg.k, "capacity_factor": cf_json(cfg.cf)},
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": r.oracle.num_threads(),
                          "kind": "oracle", "sample": r.describe(n, K)},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -530,8 +547,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16" if f16 else "f32",
         "data": "synthetic (seeded counter-based draws; 4 token batches cycled)",
-        "config": {"workload": f"{cfg.name}: 350M+MoE-128 layer" if cfg.name == "moe350m_e128"
-                   else cfg.name, "T": T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
+        "config": {"workload": workload_name(cfg), "T": T, "d": cfg.d, "f": cfg.f, "E": cfg.E,
+                   "k": cfg.k,
                    "capacity_factor": cf_json(cfg.cf),
                    "mlp_type": "residual" if cfg.residual else "standard",
                    "l2": f"inputs larger than L2: {2 * cfg.E * cfg.d * cfg.f * el / 1e9:.2f} GB of "

@@ -65,10 +65,12 @@ typedef enum {
   MOE_ERR_WORKSPACE = 3,      /* workspace missing or smaller than moe_workspace_size */
   MOE_ERR_CUDA = 4,           /* a CUDA launch or API call failed */
   MOE_ERR_TIMEOUT = 5,        /* device side: a bounded wait gave up (status word) */
-  MOE_ERR_DEVICE_BOUNDS = 6   /* device side: an index failed its bounds check (status word);
-                                 reserved: no kernel of this build raises it, and perm /
-                                 offsets / slot_of given to moe_expert_ffn / moe_combine must
-                                 be as moe_dispatch writes them */
+  MOE_ERR_DEVICE_BOUNDS = 6   /* device side: an index failed its bounds check (status word):
+                                 the expert FFN's offsets left [0, S_max] or decreased, or a
+                                 perm entry left [0, T).  The offending index is clamped (no
+                                 access leaves its buffer) and the outputs are unspecified.
+                                 moe_combine's slot_of is not checked (the call has no bound
+                                 for it): pass it as moe_dispatch writes it */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_F16 = 1 } moe_dtype;           /* activations and expert weights */
@@ -76,8 +78,10 @@ typedef enum { MOE_MLP_STANDARD = 0, MOE_MLP_RESIDUAL = 1 } moe_mlp_type;
 
 /*
  * Capacity per expert: C = ceil(cf * T / E), with cf*T and the division evaluated in
- * double.  The pages name an expert's capacity (DeepSpeed-MoE review, "Phenomenon2") but
- * give no formula; this is the capacity-factor definition.  Host only.
+ * double.  The pages define no per-expert token capacity: the "expert capacity" of the
+ * DeepSpeed-MoE review ("Phenomenon2") is the number of experts each token passes through
+ * (k here; Top2-MoE doubles it).  The token capacity of an expert is therefore a reading:
+ * the capacity-factor rule above, with overflow dropped in token order.  Host only.
  * cf = +INFINITY selects the dropless mode: C = T, so no assignment is dropped and a hot
  * expert's rows are spread over as many tiles as it needs (the single-GPU counterpart of the
  * physical expert replicas of "Fast MoE Inference via Predictive Prefetching and Expert
@@ -134,8 +138,8 @@ MOE_API moe_status moe_dispatch(const int32_t* topk_idx, int T, int E, int k, fl
  * Dispatch of one shard of a token-sharded batch, with the whole batch's capacity rule.
  * The pages have no multi-GPU data-parallel layout of this layer (their own design is expert
  * parallelism); this entry is the one exchange step that token sharding needs so that
- * routing does not depend on how the batch is split (capacity as above: the DeepSpeed-MoE
- * review, "Phenomenon2", read as ceil(cf T / E) in token order).
+ * routing does not depend on how the batch is split (capacity as moe_capacity computes it,
+ * ceil(cf T / E) of the whole batch, with drops in token order).
  *   The batch of T_global tokens is split over n_ranks callers in token order; this call
  *   holds shard `rank` (T tokens).  counts_all [n_ranks, E] int32 (device; nullable when
  *   rank == 0): the counts_raw of every shard in rank order, exchanged by the caller (for
@@ -161,6 +165,10 @@ MOE_API moe_status moe_dispatch_sharded(const int32_t* topk_idx, int T, int E, i
  *   tokens [T, d], W1 [E, d, f], W2 [E, f, d], expert_out [S_max, d]: all in `dtype`.
  *   perm, offsets: as written by moe_dispatch.  S_max >= offsets[E] bounds the slot count
  *   (min(T k, E C) always suffices).  Rows >= offsets[E] of expert_out are not written.
+ *   Bounds: the kernels clamp offsets to [0, S_max], so no row >= S_max of expert_out or of
+ *   the workspace is ever written; offsets outside that range or decreasing, and perm
+ *   entries outside [0, T), record MOE_ERR_DEVICE_BOUNDS in the workspace's status word
+ *   (moe_status_read).
  *   workspace: >= 256 + S_max * f * sizeof(dtype) bytes, rounded up to a multiple of 256
  *   (the status word, then the hidden activations H [S_max, f]); moe_workspace_size of the
  *   same layer shape is always enough for S_max = min(T k, E C).
@@ -251,9 +259,10 @@ MOE_API unsigned long long moe_kernel_launches(void);
  * activations H [S_max, f]) lives in a fixed 64 MiB array compiled into the library, which
  * every GPU that loads the library keeps until the process exits.
  *   Arguments and results: as moe_expert_ffn, without the workspace.
- *   Limit: 256 + S_max * f * sizeof(dtype) <= 64 MiB, else MOE_ERR_WORKSPACE (nothing runs).
+ *   Limit: S_max * f * sizeof(dtype) <= 64 MiB, else MOE_ERR_WORKSPACE (nothing runs).
  *   The first call on each device looks up the array's device address (with that device
- *   current); make that first call before any stream capture.
+ *   current) and keeps it; make that first call before any stream capture, and make no call
+ *   on a device after a reset of it (cudaDeviceReset), which invalidates the kept address.
  *   All calls share the one array and it keeps the last call's contents: calls that
  *   overlap on the GPU race on it (order them on one stream).  Device-side wait timeouts
  *   are not reported by this variant (it has no status word to read).

@@ -2,6 +2,7 @@
 // launch sequence of each entry point.  All device work is in the kernels of this library.
 #include <math.h>
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -39,7 +40,7 @@ constexpr int kSplitRows = 64;
 
 struct Ws {
   size_t status, logits, topk_idx, topk_w, counts, kept, offsets, perm, slot_w, slot_of, H, Hres,
-      acc32, r32, partial, partial_bytes, total;
+      acc32, r32, partial, partial_bytes, Xg, total;
 };
 
 Ws ws_layout(int T, int d, int f, int E, int k, int C, bool residual, int f_res, bool f16) {
@@ -75,6 +76,9 @@ Ws ws_layout(int T, int d, int f, int E, int k, int C, bool residual, int f_res,
     w.partial_bytes = (size_t)kMaxSplit * part_rows * cols * 4;
     w.partial = take(w.partial_bytes);
   }
+  // slot-ordered copy of the kept token rows, for batches whose experts hold more rows than
+  // one gathered tile (see run_tc_ffn)
+  w.Xg = (f16 && std::min(C, T) > kGather1Rows) ? take(std::max<size_t>(S_max, 1) * d * elt) : 0;
   w.total = off;
   return w;
 }
@@ -209,11 +213,16 @@ bool tc_plan(int rows_bound, TcPlan* p) {
   return true;
 }
 
-// Accumulator sets that fit TMEM (512 columns) for mw blocks: 2 (the epilogue overlaps the
-// next item's MMAs), else 1, else 0 (does not fit).
+// Accumulator slots of the TMEM ring (512 columns, at most 16 slots).
+uint32_t slots_for(uint32_t acc_cols) { return std::min(16u, 512u / acc_cols); }
+
+// How an item of mw blocks sits in the slot ring: 2 (room for a whole second item, so the
+// epilogue of one item overlaps all of the next item's MMAs), 1 (it fits; with more slots
+// than mw the overlap is partial), 0 (does not fit).
 int nbuf_for(int mw, uint32_t acc_cols) {
-  if (2u * (uint32_t)mw * acc_cols <= 512u) return 2;
-  if ((uint32_t)mw * acc_cols <= 512u) return 1;
+  const uint32_t n = slots_for(acc_cols);
+  if (n >= 2u * (uint32_t)mw) return 2;
+  if (n >= (uint32_t)mw) return 1;
   return 0;
 }
 
@@ -295,8 +304,8 @@ void fill_common(GemmArgs& g, const TcPlan& p, int E, int mw, int* status) {
   g.mw = mw;
   g.stages = gemm_stages_for(p.nmax, E, mw, p.smem_optin);
   g.acc_cols = p.acc_cols;
-  g.nbuf = nbuf_for(mw, p.acc_cols);
-  g.tmem_cols = pow2_at_least((uint32_t)g.nbuf * (uint32_t)mw * p.acc_cols);
+  g.nslots = slots_for(p.acc_cols);
+  g.tmem_cols = pow2_at_least(g.nslots * p.acc_cols);
   g.a_lbo = kALbo;
   g.a_sbo = kASbo;
   g.status = status;
@@ -333,16 +342,27 @@ cudaError_t stage_mark(int i, cudaStream_t s) {
 // Expert FFN stage (both GEMMs) on the tensor cores.
 moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* offsets,
                       const void* W1, const void* W2, const void* Wr1, const void* Wr2, int T,
-                      int d, int f, int E, int f_res, int S_rows, int rows_bound, __half* H,
+                      int d, int f, int E, int f_res, int S_rows, int rows_exp, int rows_bound,
+                      __half* H,
                       __half* Hres, int mode, void* out, float* acc32, float* r32,
                       const float* slot_w, const int32_t* drop_slot_of, float* partial,
-                      size_t partial_bytes, int* status, bool pdl_first, cudaStream_t s) {
+                      size_t partial_bytes, void* Xg, int* status, bool pdl_first,
+                      cudaStream_t s) {
   const bool residual = Wr1 != nullptr;
   const bool pdl = use_pdl();
-  // first GEMM: tiles of at most 64 token rows, so that items can span four weight blocks and
-  // each gathered row (a tile::gather4 TMA instruction per four rows) feeds four MMAs
+  // First GEMM.  Where an expert holds at most 64 rows: tiles of at most 64 token rows,
+  // gathered through perm by TMA (tile::gather4), so that items can span four weight blocks
+  // and each gathered row feeds four MMAs.  Where experts hold more (and the caller gave a
+  // buffer Xg of S_rows x d): the kept token rows are first copied to Xg in slot order, and
+  // one tile takes all of an expert's rows (up to 256) by 16-row boxes, so that each weight
+  // block crosses from L2 to the SM once instead of once per 64-row tile.  Row gathers move
+  // 512 bytes per TMA instruction against 2 KB per box, and at these tile heights the gather
+  // rate, not HBM, bounded the kernel (2.4B+MoE-128 layer, T = 16384, first GEMM: 4.41 ms with
+  // 64-row gathered tiles, 4.95 ms with 160-row gathered tiles).
+  const bool pregather = Xg != nullptr && rows_exp > kGather1Rows;
   TcPlan plan1, plan2;
-  if (!tc_plan(std::min(rows_bound, kGather1Rows), &plan1) || !tc_plan(rows_bound, &plan2))
+  int rows1 = pregather ? std::min(rows_exp, 256) : std::min(rows_bound, kGather1Rows);
+  if (!tc_plan(rows1, &plan1) || !tc_plan(rows_bound, &plan2))
     return MOE_ERR_CUDA;
   const int T_res = residual ? T : 0;
   const int part_rows = S_rows + T_res;
@@ -380,6 +400,8 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   if (g1.stages < 2) return MOE_ERR_UNSUPPORTED;
   g1.offsets = offsets;
   g1.perm = perm;
+  g1.S_bound = S_rows;
+  g1.n_tokens = T;
   g1.n_res_rows = residual ? T : 0;
   g1.K = d;
   g1.K_res = d;
@@ -410,20 +432,30 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   // where the shared launch would re-stream each dense weight block once per 64-row tile.
   const bool res_apart = residual && ks1 == 1 && T > plan1.nmax;
   if (res_apart) g1.n_res_rows = 0;
-  MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan1.grid, s, pdl && pdl_first));
+  CUtensorMap mXr;                       // tokens by 16-row boxes (contiguous rows)
+  if (!make_map(&mXr, tokens, d, T, 64, 16)) return MOE_ERR_CUDA;
+  if (pregather) {
+    CUtensorMap mXg;
+    if (!make_map(&mXg, Xg, d, S_dim, 64, 16)) return MOE_ERR_CUDA;
+    MOE_TRY(launch_gather_rows(tokens, perm, offsets, E, S_rows, T, d * 2, Xg, status, s,
+                               pdl && pdl_first));
+    MOE_TRY(launch_grouped_gemm1_rows(mW1, mXg, mWr1, mXr, g1, plan1.grid, s, pdl));
+  } else {
+    MOE_TRY(launch_grouped_gemm1(mW1, mX, mWr1, mX, g1, plan1.grid, s, pdl && pdl_first));
+  }
   if (ks1 > 1) MOE_TRY(launch_splitk_reduce1(g1, S_rows, T_res, f, f_res, s, pdl));
   if (res_apart) {
     TcPlan planR;
     if (!tc_plan(std::min(T, 256), &planR)) return MOE_ERR_CUDA;
     const long long resR = (T + planR.nmax - 1) / planR.nmax;
     const int mwR = choose_mw(0, f_res, resR, f_res, planR, 0);
-    CUtensorMap mXr;
-    if (!make_map(&mXr, tokens, d, T, 64, 16)) return MOE_ERR_CUDA;
     GemmArgs gr;
     fill_common(gr, planR, /*E=*/0, mwR, status);
     if (gr.stages < 2) return MOE_ERR_UNSUPPORTED;
     gr.offsets = offsets;                // no expert group: only offsets[0] (= 0) is read
     gr.perm = perm;
+    gr.S_bound = 0;
+    gr.n_tokens = T;
     gr.n_res_rows = T;
     gr.K = d;
     gr.K_res = d;
@@ -442,6 +474,8 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   if (g2.stages < 2) return MOE_ERR_UNSUPPORTED;
   g2.offsets = offsets;
   g2.perm = perm;
+  g2.S_bound = S_rows;
+  g2.n_tokens = T;
   g2.n_res_rows = residual ? T : 0;
   g2.K = f;
   g2.K_res = f_res;
@@ -512,8 +546,9 @@ moe_status expert_ffn_on_scratch(const void* tokens, const int32_t* perm, const 
                                  int* status, cudaStream_t s) {
   if (dtype == MOE_F16) {
     return run_tc_ffn(tokens, perm, offsets, W1, W2, nullptr, nullptr, T, d, f, E, 0, S_max, S_max,
-                      reinterpret_cast<__half*>(scratch), nullptr, kModeExpertOut, expert_out,
-                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, /*pdl_first=*/false, s);
+                      S_max, reinterpret_cast<__half*>(scratch), nullptr, kModeExpertOut, expert_out,
+                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, status,
+                      /*pdl_first=*/false, s);
   }
   SimtArgs a;
   memset(&a, 0, sizeof(a));
@@ -523,6 +558,8 @@ moe_status expert_ffn_on_scratch(const void* tokens, const int32_t* perm, const 
   a.W1 = static_cast<const float*>(W1);
   a.W2 = static_cast<const float*>(W2);
   a.T = T; a.d = d; a.f = f; a.E = E;
+  a.S_bound = S_max;
+  a.status = status;
   a.H = reinterpret_cast<float*>(scratch);
   a.mode = kModeExpertOut;
   a.out = static_cast<float*>(expert_out);
@@ -631,8 +668,9 @@ moe_status moe_expert_ffn(const void* tokens, const int32_t* perm, const int32_t
   MOE_TRY(cudaMemsetAsync(status, 0, sizeof(int), s));
   if (f16) {
     return run_tc_ffn(tokens, perm, offsets, W1, W2, nullptr, nullptr, T, d, f, E, 0, S_max, S_max,
-                      reinterpret_cast<__half*>(ws + kAlign), nullptr, kModeExpertOut, expert_out,
-                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, status, /*pdl_first=*/false, s);
+                      S_max, reinterpret_cast<__half*>(ws + kAlign), nullptr, kModeExpertOut, expert_out,
+                      nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, status,
+                      /*pdl_first=*/false, s);
   }
   SimtArgs a;
   memset(&a, 0, sizeof(a));
@@ -642,6 +680,8 @@ moe_status moe_expert_ffn(const void* tokens, const int32_t* perm, const int32_t
   a.W1 = static_cast<const float*>(W1);
   a.W2 = static_cast<const float*>(W2);
   a.T = T; a.d = d; a.f = f; a.E = E;
+  a.S_bound = S_max;
+  a.status = status;
   a.H = reinterpret_cast<float*>(ws + kAlign);
   a.mode = kModeExpertOut;
   a.out = static_cast<float*>(expert_out);
@@ -724,15 +764,16 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
                             slot_w, s, use_pdl()));
   }
   MOE_TRY(stage_mark(3, s));
-  const int rows_bound = std::max(std::min(C, T * k), residual ? T : 0);
+  const int rows_exp = std::min(C, T);     // rows of one expert: a token visits it at most once
+  const int rows_bound = std::max(rows_exp, residual ? T : 0);
   if (f16) {
     st = run_tc_ffn(tokens, perm, offsets, W1, W2, residual ? Wr1 : nullptr, residual ? Wr2 : nullptr,
-                    T, d, f, E, residual ? f_res : 0, S_max, rows_bound,
+                    T, d, f, E, residual ? f_res : 0, S_max, rows_exp, rows_bound,
                     reinterpret_cast<__half*>(ws + L.H),
                     residual ? reinterpret_cast<__half*>(ws + L.Hres) : nullptr, mode, out, acc32, r32,
                     slot_w, k == 1 ? slot_of : nullptr,
                     L.partial_bytes ? reinterpret_cast<float*>(ws + L.partial) : nullptr,
-                    L.partial_bytes, status, /*pdl_first=*/true, s);
+                    L.partial_bytes, L.Xg ? ws + L.Xg : nullptr, status, /*pdl_first=*/true, s);
     if (st != MOE_OK) return st;
   } else {
     SimtArgs a;
@@ -745,6 +786,8 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
     a.Wr1 = residual ? static_cast<const float*>(Wr1) : nullptr;
     a.Wr2 = residual ? static_cast<const float*>(Wr2) : nullptr;
     a.T = T; a.d = d; a.f = f; a.E = E; a.f_res = residual ? f_res : 0;
+    a.S_bound = S_max;
+    a.status = status;
     a.H = reinterpret_cast<float*>(ws + L.H);
     a.Hres = residual ? reinterpret_cast<float*>(ws + L.Hres) : nullptr;
     a.mode = mode;

@@ -1,8 +1,9 @@
 // Capacity-limited dispatch: per-expert counts, exclusive scan, slot assignment in token
 // order, overflow dropped.
 //
-// Reading of the pages (which name expert capacity in the DeepSpeed-MoE review,
-// "Phenomenon2", without a rule): capacity C = ceil(cf T / E) per expert; the assignments
+// Reading (the pages define no per-expert token capacity; the "expert capacity" of the
+// DeepSpeed-MoE review, "Phenomenon2", counts experts per token): capacity-factor rule
+// C = ceil(cf T / E) per expert; the assignments
 // (t, j) are taken token-major; an assignment's rank is the number of earlier assignments
 // to the same expert; it is kept iff rank < C; expert e owns the compact slot range
 // offsets[e] .. offsets[e] + kept[e] - 1 in token order.

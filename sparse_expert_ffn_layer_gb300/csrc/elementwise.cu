@@ -1,5 +1,6 @@
-// Bandwidth kernels around the expert GEMMs: clearing, the fp32 -> output conversion, the
-// standalone gate-weighted combine, and the bounded-wait self test.  Grids are sized in
+// Bandwidth kernels around the expert GEMMs: clearing, the slot-ordered copy of the token
+// rows, the fp32 -> output conversion, the standalone gate-weighted combine, and the
+// bounded-wait self test.  Grids are sized in
 // multiples of the SM count and use 16-byte accesses where the row length allows.
 #include "launch.h"
 
@@ -102,6 +103,30 @@ __global__ void combine_kernel(const T_* __restrict__ eo, const int32_t* __restr
   }
 }
 
+// Slot-ordered copy of the dispatched token rows: Xg[s, :] = X[perm[s], :] for every kept slot
+// s < min(offsets[E], S_bound), a warp per row with 16-byte accesses.  A perm entry outside
+// [0, T) records MOE_ERR_DEVICE_BOUNDS and gives a zero row.
+__global__ void gather_rows_kernel(const uint4* __restrict__ X, const int32_t* __restrict__ perm,
+                                   const int32_t* __restrict__ offsets, int E, int S_bound, int T,
+                                   int row_u4, uint4* __restrict__ Xg, int* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int S = min(max(offsets[E], 0), S_bound);
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int s = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; s < S; s += warps) {
+    const int t = perm[s];
+    uint4* dst = Xg + (size_t)s * row_u4;
+    if ((unsigned)t >= (unsigned)T) {
+      if (lane == 0) record_status(status, kErrBounds);
+      for (int c = lane; c < row_u4; c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const uint4* src = X + (size_t)t * row_u4;
+    for (int c = lane; c < row_u4; c += 32) dst[c] = src[c];
+  }
+}
+
 __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -178,6 +203,15 @@ cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d
                                   bool pdl) {
   const size_t n = (size_t)(S_max + T_res) * d;
   return launch_k(splitk_reduce2_kernel, grid_for(n, 256), 256, 0, s, pdl, g, S_max, T_res, d);
+}
+
+cudaError_t launch_gather_rows(const void* X, const int32_t* perm, const int32_t* offsets, int E,
+                               int S_bound, int T, int row_bytes, void* Xg, int* status,
+                               cudaStream_t s, bool pdl) {
+  // a warp per row, at most 8 CTAs of 128 threads per SM
+  return launch_k(gather_rows_kernel, grid_for((size_t)S_bound * 32, 128), 128, 0, s, pdl,
+                  static_cast<const uint4*>(X), perm, offsets, E, S_bound, T, row_bytes / 16,
+                  static_cast<uint4*>(Xg), status);
 }
 
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s) {

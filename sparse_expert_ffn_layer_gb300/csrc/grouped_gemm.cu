@@ -34,6 +34,7 @@ constexpr int kThreads = 192;
 constexpr int kBM = 128;          // MMA M (weight rows per accumulator)
 constexpr int kBK = 64;           // K per pipeline stage (one 128-byte swizzle span of f16)
 constexpr int kABytes = kBM * kBK * 2;   // one 128-row A block per stage; an item has mw of them
+constexpr int kMaxSlots = 16;     // TMEM accumulator slots (512 columns / at least 32 each)
 
 struct SmemLayout {
   uint32_t stage_bytes, b_off, bars_off, misc_off, rows_off, total;
@@ -45,7 +46,7 @@ __host__ __device__ inline SmemLayout smem_layout(int nmax, int stages, int E, i
   L.stage_bytes = L.b_off + (uint32_t)nmax * 128u;
   uint32_t off = (uint32_t)stages * L.stage_bytes;
   L.bars_off = off;
-  off += (uint32_t)(2 * stages + 4) * 8u;
+  off += (uint32_t)(2 * stages + 2 * kMaxSlots) * 8u;
   L.misc_off = off;
   off += 16u + 8u * (uint32_t)(E + 1);       // tmem base, abort flag, chunk prefix, offsets
   L.rows_off = off;
@@ -82,7 +83,7 @@ __device__ __forceinline__ Tile decode(int i, const GemmArgs& a, const int32_t* 
     const int chunk = local - t.mt * chunks;
     t.res = 0;
     t.e = lo;
-    const int kept = offs[lo + 1] - offs[lo];
+    const int kept = max(0, offs[lo + 1] - offs[lo]);
     t.row0 = offs[lo] + chunk * a.nmax;
     t.n = min(a.nmax, kept - chunk * a.nmax);
     t.K = a.K;
@@ -112,8 +113,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int mw = kMW;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off);
   uint64_t* empty = full + a.stages;
-  uint64_t* acc_full = empty + a.stages;     // [2]
-  uint64_t* acc_empty = acc_full + 2;        // [2]
+  // TMEM accumulators form a ring of nslots slots of acc_cols columns.  Item j (the j-th
+  // item of this CTA) accumulates its mw weight blocks in slots (j mw + h) mod nslots; the
+  // MMA warp waits for a slot to be drained (acc_empty[slot]) just before the first MMA into
+  // it, and the epilogue releases each slot as soon as it has read it, so the next item's
+  // MMAs overlap the epilogue whenever nslots > mw.  acc_full[j mod nslots] completes when
+  // item j's MMAs are done.
+  uint64_t* acc_full = empty + a.stages;     // [nslots]
+  uint64_t* acc_empty = acc_full + kMaxSlots;  // [nslots]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.misc_off + 16);
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < a.nslots; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 128);
     }
@@ -150,13 +157,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
   // chunk prefix over experts (warp 2), E <= 1024
   if (warp == 2) {
-    for (int e = lane; e <= a.E; e += 32) soffs[e] = a.offsets[e];
+    // offsets clamped to [0, S_bound]: offsets[E] beyond the caller's S_max cannot make a
+    // tile write past H or the output, and decreasing offsets give empty groups (kept is
+    // taken as max(0, .) below); either records MOE_ERR_DEVICE_BOUNDS
+    bool bad = false;
+    for (int e = lane; e <= a.E; e += 32) {
+      const int o = a.offsets[e];
+      soffs[e] = min(max(o, 0), a.S_bound);
+      bad |= soffs[e] != o;
+    }
     __syncwarp();
+    for (int e = lane; e < a.E; e += 32) bad |= soffs[e + 1] < soffs[e];
+    if (bad) record_status(a.status, kErrBounds);
     const int per = (a.E + 31) / 32;
     const int e_lo = lane * per, e_hi = min(a.E, e_lo + per);
     int local = 0;
     for (int e = e_lo; e < e_hi; ++e) {
-      const int kept = soffs[e + 1] - soffs[e];
+      const int kept = max(0, soffs[e + 1] - soffs[e]);
       local += (kept + a.nmax - 1) / a.nmax;
     }
     int incl = local;
@@ -168,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = incl - local;
     for (int e = e_lo; e < e_hi; ++e) {
       prefix[e] = run;
-      const int kept = soffs[e + 1] - soffs[e];
+      const int kept = max(0, soffs[e + 1] - soffs[e]);
       run += (kept + a.nmax - 1) / a.nmax;
     }
     if (lane == 31) prefix[a.E] = incl;
@@ -197,7 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) {
           const int r = 4 * (lane + 32 * h) + q;
           const int src = t.row0 + (r < t.n ? r : 0);
-          rows[h][q] = t.res ? src : a.perm[src];
+          int tok = t.res ? src : a.perm[src];
+          if ((unsigned)tok >= (unsigned)a.n_tokens) {   // not a token of this batch
+            record_status(a.status, kErrBounds);
+            tok = 0;
+          }
+          rows[h][q] = tok;
         }
     };
     int rows[2][4], rows_next[2][4];
@@ -268,14 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile t = decode(i / ksplit, a, prefix, soffs);
       const int ks = i - (i / ksplit) * ksplit;
       const int npad = max(16, (t.n + 15) & ~15);
-      const int buf = local % a.nbuf;
-      const uint32_t use = (uint32_t)(local / a.nbuf) & 1u;
+      const uint32_t blk0 = (uint32_t)local * mw;        // ring position of block 0
+      uint32_t d_tmem[mw];
+#pragma unroll
+      for (int h = 0; h < mw; ++h) d_tmem[h] = tmem_base + ((blk0 + h) % a.nslots) * a.acc_cols;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait_bounded(&acc_empty[buf], use ^ 1u, abort_flag, a.status, a.wait_ns);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * mw) * a.acc_cols;
       const uint32_t idesc = idesc_f16(kBM, npad, 1, 0);
       const int nkb = t.K / kBK;
       const int kb0 = ks * nkb / ksplit, kb1 = (ks + 1) * nkb / ksplit;
@@ -292,21 +311,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
 #pragma unroll
             for (int h = 0; h < mw; ++h) {             // same token rows, mw weight blocks
+              if (kb == kb0 && kk == 0 && ok) {
+                // first MMA into this block: its slot must have been drained by the epilogue
+                const uint32_t blk = blk0 + h;
+                ok = mbar_wait_bounded(&acc_empty[blk % a.nslots], ((blk / a.nslots) & 1u) ^ 1u,
+                                       abort_flag, a.status, a.wait_ns);
+                tc_fence_after();
+              }
+              if (!ok) break;
               const uint64_t ad = smem_desc(a0 + h * kABytes + kk * 2048, a.a_lbo, a.a_sbo, 2);
-              tc_mma_f16(d_tmem + (uint32_t)h * a.acc_cols, ad, bd, idesc,
-                         (kb != kb0 || kk != 0) ? 1u : 0u);
+              tc_mma_f16(d_tmem[h], ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
             }
           }
-          tc_commit(&empty[stage]);        // frees the stage once these MMAs have read it
+          if (ok) tc_commit(&empty[stage]);  // frees the stage once these MMAs have read it
         }
-        __syncwarp();
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
         if (++stage == a.stages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(&acc_full[buf]);
+      if (lane == 0) tc_commit(&acc_full[local % a.nslots]);
       __syncwarp();
     }
   } else {
@@ -335,8 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++local) {
       const Tile t = decode(i / ksplit, a, prefix, soffs);
       const int ks = i - (i / ksplit) * ksplit;
-      const int buf = local % a.nbuf;
-      const uint32_t use = (uint32_t)(local / a.nbuf) & 1u;
       // second GEMM: each warp stages the tile's tokens and gate weights in its own shared
       // memory while the accumulator is still being computed (a load per row per warp
       // instead of one per row per thread; warp-private, so no cross-warp barrier)
@@ -351,15 +376,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       bool ok = true;
-      if (lane == 0) ok = mbar_wait_bounded(&acc_full[buf], use, abort_flag, a.status, a.wait_ns);
+      if (lane == 0)
+        ok = mbar_wait_bounded(&acc_full[local % a.nslots], (uint32_t)(local / a.nslots) & 1u,
+                               abort_flag, a.status, a.wait_ns);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
       for (int h = 0; h < mw; ++h) {
       const int m = (t.mt * mw + h) * kBM + row_in_tile;
-      const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) +
-                             (uint32_t)(buf * mw + h) * a.acc_cols;
+      const uint32_t slot = ((uint32_t)local * mw + h) % a.nslots;
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + slot * a.acc_cols;
       for (int c0 = 0; c0 < t.n; c0 += 16) {
         float v[16];
         tmem_ld16(taddr + (uint32_t)c0, v);
@@ -389,9 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      }
       tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
+      mbar_arrive(&acc_empty[slot]);       // this block's slot may take the next MMAs
+      }
     }
   }
 

@@ -52,9 +52,12 @@ enum : int {
 
 struct GemmArgs {
   // groups
-  const int32_t* offsets;   // [E + 1] slot offsets per expert
+  const int32_t* offsets;   // [E + 1] slot offsets per expert, clamped to [0, S_bound] on load
   const int32_t* perm;      // [S] token of each slot
   int E;
+  int S_bound;              // rows of H / of the slot-ordered output: no expert row >= it is
+                            // read or written, whatever offsets[E] says
+  int n_tokens;             // rows of the gathered token matrix (a perm entry must be below)
   int n_res_rows;           // rows of the residual group (T), 0 when absent
   int K, K_res;             // shared dimension of expert / residual tiles
   int mt_exp, mt_res;       // M items (of mw x 128 rows) per expert / residual row tile
@@ -64,8 +67,9 @@ struct GemmArgs {
   int nmax;                 // rows per tile, multiple of 16, <= 256
   int stages;               // pipeline depth
   uint32_t acc_cols;        // TMEM columns per accumulator (nmax rounded up to 32)
-  int nbuf;                 // accumulator sets (2: the epilogue overlaps the next item)
-  uint32_t tmem_cols;       // TMEM columns allocated: power of two >= nbuf * mw * acc_cols
+  uint32_t nslots;          // accumulator slots in the TMEM ring (>= mw, <= 16); with more
+                            // than mw the epilogue of an item overlaps the next item's MMAs
+  uint32_t tmem_cols;       // TMEM columns allocated: power of two >= nslots * acc_cols
   uint32_t a_lbo, a_sbo;    // A (M-major, 128-byte swizzle) descriptor byte offsets
   int mode;                 // kMode* (second GEMM)
   // first GEMM outputs
@@ -143,6 +147,7 @@ struct SimtArgs {
   const float* Wr1;         // [d, f_res] or null
   const float* Wr2;         // [f_res, d]
   int T, d, f, E, f_res;
+  int S_bound;              // expert slots are clamped to [0, S_bound) (the S_max of H)
   float* H;                 // [S_max, f]
   float* Hres;              // [T, f_res]
   int mode;                 // kMode*
@@ -150,11 +155,16 @@ struct SimtArgs {
   float* acc32;             // kModeAccum: [T, d]
   float* r32;               // residual: [T, d]
   const float* slot_w;
+  int* status;              // device status word for MOE_ERR_DEVICE_BOUNDS, or null
 };
 cudaError_t launch_simt_ffn1(const SimtArgs& a, int S_max, cudaStream_t s);
 cudaError_t launch_simt_ffn2(const SimtArgs& a, int S_max, cudaStream_t s);
 
 // elementwise kernels
+// Xg[s] = X[perm[s]] for the kept slots s < min(offsets[E], S_bound) (row_bytes % 16 == 0).
+cudaError_t launch_gather_rows(const void* X, const int32_t* perm, const int32_t* offsets, int E,
+                               int S_bound, int T, int row_bytes, void* Xg, int* status,
+                               cudaStream_t s, bool pdl = false);
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
 cudaError_t launch_zero_dropped_rows(const int32_t* slot_of, int T, int k, int d, int dtype_f16,
                                      void* out, cudaStream_t s);

@@ -5,7 +5,8 @@
 // the fp32 logit chain acc = fmaf(x[t,i], Wg[i,e], acc) in ascending i from +0 (gating
 // function: DeepSpeed-MoE review, "MoE based NLG Model Architecture"), top-k on the logits
 // with ties to the lower index and the softmax weights (topk.cuh), then the token-order
-// capacity rule with compact slots (capacity: same review, "Phenomenon2").
+// capacity rule with compact slots (C = ceil(cf T / E), a reading: the pages give no
+// per-expert token capacity).
 //
 // Shape of the work.  At decode sizes the gate is latency-bound: T * E chains of d dependent
 // FMAs and a Wg read of d * E * 4 bytes.  Each CTA owns 8 experts x 32 tokens (one chain per

@@ -21,8 +21,13 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs a) {
     rows = a.T;
     row0 = 0;
   } else {
-    row0 = a.offsets[g];
-    rows = a.offsets[g + 1] - row0;
+    // slot range of expert g, clamped to [0, S_bound): offsets that run past the caller's
+    // S_max leave the rows beyond it uncomputed instead of writing past H or the output
+    row0 = min(max(a.offsets[g], 0), a.S_bound);
+    rows = min(max(a.offsets[g + 1], row0), a.S_bound) - row0;
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 &&
+        (row0 != a.offsets[g] || row0 + rows != a.offsets[g + 1]))
+      record_status(a.status, kErrBounds);
   }
   const int r0 = blockIdx.z * kR;
   if (r0 >= rows) return;
@@ -47,7 +52,9 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs a) {
       if (r < rows && kk < kc) {
         if (kStage == 1) {
           const int tok = res ? r : a.perm[row0 + r];
-          v = a.x[(size_t)tok * a.d + k0 + kk];
+          // a token index outside [0, T) reads as a zero row and records the error
+          if ((unsigned)tok < (unsigned)a.T) v = a.x[(size_t)tok * a.d + k0 + kk];
+          else record_status(a.status, kErrBounds);
         } else {
           v = res ? a.Hres[(size_t)r * a.f_res + k0 + kk] : a.H[(size_t)(row0 + r) * a.f + k0 + kk];
         }

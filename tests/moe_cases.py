@@ -85,27 +85,49 @@ class Case:
                                          float(np.float32(self.cfg.cf)))
         return self._routing
 
-    def reference_rows(self, rows):
+    def reference_rows(self, rows, max_experts=24):
+        """Oracle output of the listed rows.  Rows are taken in groups whose kept assignments
+        use at most max_experts experts, so that only those experts' weights are drawn on the
+        host at a time (the largest layers hold 26 GB of expert weights)."""
         r = self.routing()
         rows = np.asarray(rows, dtype=np.int32)
-        used = set()
-        for t in rows:
-            for j in range(self.cfg.k):
-                if r.disp.slot_of[t, j] >= 0:
-                    used.add(int(r.topk_idx[t, j]))
-        w1, w2 = synth.expert_slices(self.cfg, sorted(used), self.seed)
-        return oracle.combine_rows(self.tokens, r, w1, w2, self.Wr1, self.Wr2, rows=rows)
+        need = [sorted({int(r.topk_idx[t, j]) for j in range(self.cfg.k)
+                        if r.disp.slot_of[t, j] >= 0}) for t in rows]
+        order = sorted(range(rows.size), key=lambda i: (need[i] or [-1])[0])
+        out = np.empty((rows.size, self.cfg.d), np.float64)
+
+        def flush(group, experts):
+            if not group:
+                return
+            w1, w2 = synth.expert_slices(self.cfg, sorted(experts), self.seed)
+            out[group] = oracle.combine_rows(self.tokens, r, w1, w2, self.Wr1, self.Wr2,
+                                             rows=rows[group])
+
+        group, experts = [], set()
+        for i in order:
+            union = experts | set(need[i])
+            if len(union) > max_experts and group:
+                flush(group, experts)
+                group, union = [], set(need[i])
+            group.append(i)
+            experts = union
+        flush(group, experts)
+        return out
 
 
-def sample_rows(r, T, n_random=24, seed=0):
-    """First and last tokens, some dropped tokens, one kept token per active expert (capped),
-    and random tokens."""
+def sample_rows(r, T, n_random=512, seed=0, n_dropped=64):
+    """Rows compared at sizes where the oracle cannot take every row: the first and last
+    tokens, up to n_dropped tokens with a dropped assignment, for every active expert the
+    first and the last token it kept (the last one sits at the capacity boundary), and
+    n_random random tokens."""
     rng = np.random.default_rng(seed)
     rows = {0, T - 1}
-    dropped = np.where((r.disp.slot_of < 0).all(axis=1))[0]
-    rows.update(dropped[:8].tolist())
-    kept_any = np.where((r.disp.slot_of >= 0).any(axis=1))[0]
-    for e in np.unique(r.topk_idx[kept_any, 0])[:8]:
-        rows.add(int(kept_any[r.topk_idx[kept_any, 0] == e][0]))
+    dropped = np.where((r.disp.slot_of < 0).any(axis=1))[0]
+    rows.update(dropped[:n_dropped].tolist())
+    offs, perm = r.disp.offsets, r.disp.perm
+    for e in range(offs.size - 1):
+        if offs[e + 1] > offs[e]:
+            rows.add(int(perm[offs[e]]))
+            rows.add(int(perm[offs[e + 1] - 1]))
     rows.update(rng.choice(T, size=min(T, n_random), replace=False).tolist())
     return np.array(sorted(rows), dtype=np.int32)

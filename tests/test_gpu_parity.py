@@ -174,15 +174,17 @@ def test_dispatch_sharded_bit_exact(m, T, E, k, cf, cuts):
 
 
 # ------------------------------------------------------------------------------ whole layer
+# (layer, T, rows): rows None compares every row, an int n compares sample_rows with n
+# random rows besides the first / last, dropped and per-expert boundary rows
 LAYER_CASES = [
     ("tiny_fp32", 128, None), ("tiny_fp32", 1, None), ("tiny_fp32", 37, None),
     ("moe350m_e128", 1, None), ("moe350m_e128", 8, None), ("moe350m_e128", 64, None),
-    ("moe350m_e128", 512, 40),
-    ("moe1p3b_e128_zipf", 16, None), ("moe1p3b_e128_zipf", 256, 40),
-    ("prmoe_e64", 64, 24), ("prmoe_e128", 64, 24),
-    ("moe2p4b_e128_top2", 1, None), ("moe2p4b_e128_top2", 32, 10),
-    ("moe2p4b_e128_top2_zipf", 32, 10),
-    ("top2_e64", 64, 24), ("top2_e128", 2048, 24),
+    ("moe350m_e128", 512, None),
+    ("moe1p3b_e128_zipf", 16, None), ("moe1p3b_e128_zipf", 256, None),
+    ("prmoe_e64", 64, None), ("prmoe_e128", 64, None),
+    ("moe2p4b_e128_top2", 1, None), ("moe2p4b_e128_top2", 32, None),
+    ("moe2p4b_e128_top2_zipf", 32, None),
+    ("top2_e64", 64, None), ("top2_e128", 2048, 512),
     # decode batches whose slots plus residual rows fit the split-K path (residual group split)
     ("prmoe_e64", 16, None), ("tiny_prmoe_e8", 24, None),
 ]
@@ -206,6 +208,7 @@ def test_layer_forward(m, name, T, n_rows):
 
 
 @pytest.mark.parametrize("name,T,cf", [("moe1p3b_e128_zipf", 256, 2.0), ("moe1p3b_e128_zipf", 8192, 1.0),
+                                       ("moe1p3b_e128_zipf", 8192, 2.0),
                                        ("prmoe_e128", 2048, 1.0), ("prmoe_e64", 2048, 1.25)])
 def test_layer_forward_capacity_and_residual(m, name, T, cf):
     cfg = synth.CONFIGS[name].at(cf=cf)
@@ -213,15 +216,15 @@ def test_layer_forward_capacity_and_residual(m, name, T, cf):
     out, idx, slot = case.forward(m)
     r = case.routing()
     assert np.array_equal(idx, r.topk_idx) and np.array_equal(slot, r.disp.slot_of)
-    rows = sample_rows(r, T, 24)
+    rows = sample_rows(r, T)
     ok, err, bound = within_tol(out[rows], case.reference_rows(rows))
     assert ok, f"max err {err:.3e} > bound {bound:.3e}"
     del case
     torch.cuda.empty_cache()
 
 
-def test_layer_bench_workload(m):
-    """The benchmark's configuration: 350M+MoE-128 layer, T = 4096, top-1, cf 1.25."""
+def test_layer_350m_every_row(m):
+    """350M+MoE-128 layer, T = 4096, top-1, cf 1.25: every row against the oracle."""
     cfg = synth.CONFIGS["moe350m_e128"]
     case = Case(cfg, 4096, seed=0)
     out, idx, slot = case.forward(m)
@@ -230,21 +233,58 @@ def test_layer_bench_workload(m):
     assert np.isfinite(out).all()
     dropped = np.where(slot[:, 0] < 0)[0]
     assert np.all(out[dropped] == 0.0)              # top-1 drops give exact zeros
-    rows = sample_rows(r, 4096, 48)
+    rows = np.arange(4096, dtype=np.int32)
     ok, err, bound = within_tol(out[rows], case.reference_rows(rows))
     assert ok, f"max err {err:.3e} > bound {bound:.3e}"
 
 
-@pytest.mark.parametrize("name,T", [("moe2p4b_e128_top2", 1024), ("moe2p4b_e128_top2_zipf", 16384)])
+@pytest.mark.parametrize("name,T", [("moe2p4b_e128_top2", 16384), ("moe2p4b_e128_top2", 1024),
+                                    ("moe2p4b_e128_top2_zipf", 16384),
+                                    ("moe2p4b_e128_top2_zipf", 1024)])
 def test_layer_forward_largest(m, name, T):
+    """The 2.4B+MoE-128 top-2 layer (26 GB of experts), uniform and Zipf(1.2) routing; the
+    uniform T = 16384 batch is the benchmark's workload."""
     cfg = synth.CONFIGS[name]
     case = Case(cfg, T, seed=0)
     out, idx, slot = case.forward(m)
     r = case.routing()
     assert np.array_equal(idx, r.topk_idx) and np.array_equal(slot, r.disp.slot_of)
-    rows = sample_rows(r, T, 6)
+    assert np.isfinite(out).all()
+    rows = sample_rows(r, T)
     ok, err, bound = within_tol(out[rows], case.reference_rows(rows))
     assert ok, f"max err {err:.3e} > bound {bound:.3e}"
+    del case
+    torch.cuda.empty_cache()
+
+
+def test_layer_graph_replay_matches_direct_call(m):
+    """The benchmark times the layer as a CUDA graph replayed back to back over several token
+    batches; at the benchmark's workload (2.4B+MoE-128, top-2, T = 16384) every replay must
+    give the direct call's output bit for bit, whatever batch ran before it."""
+    cfg = synth.CONFIGS["moe2p4b_e128_top2"]
+    T = 16384
+    case = Case(cfg, T, seed=0)
+    other = torch.from_numpy(synth.fill((T, cfg.d), synth.F16, 0, synth.TID_TOKENS + (1 << 8),
+                                        cfg.tok_sigma)).cuda()
+    want, _, _ = case.forward(m)
+    ws = case.workspace(m)
+    outs = [torch.empty((T, cfg.d), dtype=torch.float16, device="cuda") for _ in range(2)]
+    srcs = [case.d_tokens, other]
+    cap = torch.cuda.Stream()
+    graphs = []
+    for b in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            m.moe_layer_forward(srcs[b], case.d_Wg, case.d_W1, case.d_W2, cfg.k, cfg.cf, outs[b],
+                                ws)
+        graphs.append(g)
+    for rep in range(3):
+        graphs[1].replay()
+        graphs[0].replay()
+        torch.cuda.synchronize()
+        assert m.moe_status_read(ws) == m.MOE_OK
+        got = outs[0].float().cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), rep
     del case
     torch.cuda.empty_cache()
 
@@ -263,7 +303,7 @@ def test_layer_forward_dropless(m, name, T):
     assert np.array_equal(idx, r.topk_idx) and np.array_equal(slot, r.disp.slot_of)
     hot = int(np.argmax(r.disp.kept))
     hot_tokens = r.disp.perm[r.disp.offsets[hot]:r.disp.offsets[hot + 1]]
-    rows = np.unique(np.concatenate([sample_rows(r, T, 6),
+    rows = np.unique(np.concatenate([sample_rows(r, T, 128),
                                      hot_tokens[[0, len(hot_tokens) // 2, -1]]])).astype(np.int32)
     ok, err, bound = within_tol(out[rows], case.reference_rows(rows))
     assert ok, f"max err {err:.3e} > bound {bound:.3e}"
@@ -349,10 +389,9 @@ def test_closed_form_zero_gate_and_zero_tokens(m):
 
 @pytest.mark.parametrize("k", [1, 2])
 def test_layer_routing_with_tied_gate_columns(m, k):
-    """Experts whose gate columns are identical tie exactly on every token.  The batch is
-    large enough for the tensor-core gate, whose candidates are re-evaluated with the exact
-    chain: the tie must go to the lower index, as in the oracle (top-2: the expert and its
-    duplicate)."""
+    """Experts whose gate columns are identical tie exactly on every token (the tiled gate's
+    fp32 chains give them bit-identical logits): the tie must go to the lower index, as in
+    the oracle (top-2: the expert and its duplicate)."""
     cfg = synth.CONFIGS["moe350m_e128"].at(k=k)
     T = 256
     Wg = synth.fill((cfg.d, cfg.E), synth.F32, 7, synth.TID_WG, cfg.w_sigma)
@@ -364,9 +403,43 @@ def test_layer_routing_with_tied_gate_columns(m, k):
     assert np.all(idx[:, 0] < 64)
     if k == 2:
         assert np.array_equal(idx[:, 1], idx[:, 0] + 64)
-    rows = sample_rows(r, T, 8)
+    rows = np.arange(T, dtype=np.int32)
     ok, err, bound = within_tol(out[rows], case.reference_rows(rows))
     assert ok, f"max err {err:.3e} > bound {bound:.3e}"
+
+
+@pytest.mark.parametrize("name", ["moe350m_e128", "tiny_fp32"])
+def test_expert_ffn_index_checks(m, name):
+    """Caller-supplied offsets that run past S_max, or a perm entry outside [0, T): no row at
+    or beyond S_max is written, the context stays usable, and the status word reads
+    MOE_ERR_DEVICE_BOUNDS; in-range indices read MOE_OK."""
+    cfg = synth.CONFIGS[name].at(E=4)
+    T = 96
+    case = Case(cfg, T, seed=11)
+    ws = case.workspace(m)
+    perm = torch.arange(T, dtype=torch.int32, device="cuda")
+    offs = torch.tensor([0, 24, 48, 72, 96], dtype=torch.int32, device="cuda")
+    tdt = case.d_W1.dtype
+    ref = torch.zeros((T, cfg.d), dtype=tdt, device="cuda")
+    m.moe_expert_ffn(case.d_tokens, perm, offs, case.d_W1, case.d_W2, T, ref, ws)
+    assert m.moe_status_read(ws) == m.MOE_OK
+    S_max = 40
+    got = torch.full((T, cfg.d), 7.0, dtype=tdt, device="cuda")
+    m.moe_expert_ffn(case.d_tokens, perm, offs, case.d_W1, case.d_W2, S_max, got, ws)
+    assert m.moe_status_read(ws) == m.MOE_ERR_DEVICE_BOUNDS
+    assert torch.all(got[S_max:] == 7.0)
+    ok, err, bound = within_tol(got[:S_max].float().cpu().numpy(),
+                                ref[:S_max].float().cpu().numpy().astype(np.float64))
+    assert ok, f"max err {err:.3e} > {bound:.3e}"
+    bad = perm.clone()
+    bad[5] = T + 1000
+    bad[6] = -3
+    m.moe_expert_ffn(case.d_tokens, bad, offs, case.d_W1, case.d_W2, T, got, ws)
+    assert m.moe_status_read(ws) == m.MOE_ERR_DEVICE_BOUNDS
+    assert torch.isfinite(got.float()).all()
+    m.moe_expert_ffn(case.d_tokens, perm, offs, case.d_W1, case.d_W2, T, got, ws)
+    assert m.moe_status_read(ws) == m.MOE_OK
+    assert torch.equal(got, ref)
 
 
 def test_empty_batch_is_a_no_op(m):

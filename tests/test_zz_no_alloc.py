@@ -55,15 +55,71 @@ def test_noalloc_matches_workspace_variant_on_consecutive_calls():
         torch.cuda.empty_cache()
 
 
-def test_noalloc_rejects_sizes_beyond_its_scratch():
+def _at_the_limit_case(E=8):
+    """350M+MoE-128 expert shape (d 1024, f 4096) with S_max rows of H filling the 64 MiB
+    scratch exactly: every token in one slot, E equal expert groups."""
+    cfg = synth.CONFIGS["moe350m_e128"].at(E=E)
+    S_max = (64 << 20) // (cfg.f * 2)
+    case = Case(cfg, S_max, seed=9)
+    perm = torch.arange(S_max, dtype=torch.int32, device="cuda")
+    offs = torch.arange(0, S_max + 1, S_max // E, dtype=torch.int32, device="cuda")
+    return case, perm, offs, S_max
+
+
+def test_noalloc_at_its_limit_and_rejects_beyond():
     m = lib()
-    cfg = synth.CONFIGS["moe350m_e128"]
-    tok = torch.zeros((8, cfg.d), dtype=torch.float16, device="cuda")
-    w1 = torch.zeros((1, cfg.d, cfg.f), dtype=torch.float16, device="cuda")
-    w2 = torch.zeros((1, cfg.f, cfg.d), dtype=torch.float16, device="cuda")
-    i32 = torch.zeros(16, dtype=torch.int32, device="cuda")
-    out = torch.zeros((16, cfg.d), dtype=torch.float16, device="cuda")
-    too_many = (64 << 20) // (cfg.f * 2)            # rows of H that no longer fit with the status
+    case, perm, offs, S_max = _at_the_limit_case()
+    d = case.cfg.d
+    ref = torch.zeros((S_max, d), dtype=torch.float16, device="cuda")
+    m.moe_expert_ffn(case.d_tokens, perm, offs, case.d_W1, case.d_W2, S_max, ref, case.workspace(m))
+    got = torch.full((S_max, d), float("nan"), dtype=torch.float16, device="cuda")
+    m.moe_expert_ffn_noalloc(case.d_tokens, perm, offs, case.d_W1, case.d_W2, S_max, got)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+    # one row more than the scratch holds: rejected before anything runs
     with pytest.raises(m.MoeError) as ei:
-        m.moe_expert_ffn_noalloc(tok, i32, i32, w1, w2, too_many, out)
+        m.moe_expert_ffn_noalloc(case.d_tokens, perm, offs, case.d_W1, case.d_W2, S_max + 1, got)
     assert ei.value.code == m.MOE_ERR_WORKSPACE
+
+
+def test_noalloc_allocates_no_device_memory():
+    """The device's free memory (cudaMemGetInfo, which also sees allocations outside torch's
+    allocator) is the same before and after a run of calls; one call first so that lazily
+    loaded kernels and the scratch array are resident before the first reading."""
+    m = lib()
+    case, perm, offs, S_max = _at_the_limit_case()
+    out = torch.empty((S_max, case.cfg.d), dtype=torch.float16, device="cuda")
+    m.moe_expert_ffn_noalloc(case.d_tokens, perm, offs, case.d_W1, case.d_W2, S_max, out)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        m.moe_expert_ffn_noalloc(case.d_tokens, perm, offs, case.d_W1, case.d_W2, S_max, out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+
+
+def test_noalloc_never_writes_rows_beyond_s_max():
+    """offsets that run past S_max: the rows below S_max are computed, none at or beyond it is
+    written (the output buffer's tail keeps its sentinel), and the shared scratch is not
+    overrun (a following in-range call still matches the workspace variant)."""
+    m = lib()
+    cfg = synth.CONFIGS["moe350m_e128"].at(E=4)
+    T = 96
+    case = Case(cfg, T, seed=10)
+    perm = torch.arange(T, dtype=torch.int32, device="cuda")
+    offs = torch.tensor([0, 24, 48, 72, 96], dtype=torch.int32, device="cuda")
+    S_max = 40                                      # offsets[E] = 96 > S_max
+    got = torch.full((T, cfg.d), 7.0, dtype=torch.float16, device="cuda")
+    m.moe_expert_ffn_noalloc(case.d_tokens, perm, offs, case.d_W1, case.d_W2, S_max, got)
+    ref = torch.zeros((T, cfg.d), dtype=torch.float16, device="cuda")
+    m.moe_expert_ffn(case.d_tokens, perm, offs, case.d_W1, case.d_W2, T, ref, case.workspace(m))
+    torch.cuda.synchronize()
+    assert torch.all(got[S_max:] == 7.0)
+    ok, err, bound = within_tol(got[:S_max].float().cpu().numpy(),
+                                ref[:S_max].float().cpu().numpy().astype(np.float64))
+    assert ok, f"max err {err:.3e} > {bound:.3e}"
+    again = torch.zeros((T, cfg.d), dtype=torch.float16, device="cuda")
+    m.moe_expert_ffn_noalloc(case.d_tokens, perm, offs, case.d_W1, case.d_W2, T, again)
+    torch.cuda.synchronize()
+    assert torch.equal(again, ref)
