@@ -200,8 +200,13 @@ MOE_API moe_status moe_combine(const void* expert_out, const int32_t* slot_of, c
  *   topk_idx_out nullable [T, k], slot_of_out nullable [T, k]: routing, as moe_gate_topk /
  *   moe_dispatch define it.
  *   workspace >= moe_workspace_size(...) bytes; contents need no initialisation.
- * Deterministic: repeated calls give identical bits (fp32 sums of at most two addends
- * commute exactly; larger sums use a fixed order).
+ *   out must not overlap tokens or the workspace: it is cleared before the experts' outputs
+ *   are added into it.
+ * Deterministic: repeated calls give identical bits.  Top-1 standard layers write each
+ * output row once.  Where an output element has two addends (top-2, or one expert plus the
+ * residual MLP), each is rounded to `dtype` and added into the cleared output: 0 + a is exact
+ * and a + b commutes, so the order of the additions does not matter.  Top-2 with the residual
+ * MLP (three addends) sums in fp32 in a fixed order and rounds once.
  */
 MOE_API moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1, const void* W2,
                              const void* Wr1, const void* Wr2, moe_dtype dtype, int T, int d,

@@ -46,7 +46,7 @@ struct Ws {
 Ws ws_layout(int T, int d, int f, int E, int k, int C, bool residual, int f_res, bool f16) {
   const size_t elt = f16 ? 2 : 4;
   const size_t S_max = (size_t)std::min<long long>((long long)T * k, (long long)E * C);
-  const bool accum = k == 2 || residual;
+  const bool accum = k == 2 && residual;     // three addends per output: fp32, fixed order
   Ws w;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -413,8 +413,11 @@ moe_status run_tc_ffn(const void* tokens, const int32_t* perm, const int32_t* of
   g1.hres_out = Hres;
   g1.ldhres = f_res;
   if (mode == kModeAccum) {
-    g1.zero_f32 = acc32;
-    g1.zero_f32_n = (size_t)T * d;
+    g1.zero_buf = acc32;
+    g1.zero_bytes = (size_t)T * d * 4;
+  } else if (mode == kModeSum) {
+    g1.zero_buf = out;                   // the second GEMM adds into it
+    g1.zero_bytes = (size_t)T * d * 2;
   }
   if (mode == kModeDirect && drop_slot_of) {
     g1.drop_slot_of = drop_slot_of;
@@ -741,7 +744,10 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
   int32_t* slot_of = slot_of_out ? slot_of_out : reinterpret_cast<int32_t*>(ws + L.slot_of);
   float* acc32 = L.acc32 ? reinterpret_cast<float*>(ws + L.acc32) : nullptr;
   float* r32 = L.r32 ? reinterpret_cast<float*>(ws + L.r32) : nullptr;
-  const int mode = (k == 1 && !residual) ? kModeDirect : kModeAccum;
+  // top-1 standard: each output row written once; top-2 or one expert plus the residual MLP:
+  // two addends summed in place (order-independent); top-2 plus the residual MLP: three
+  // addends, summed in fp32 in a fixed order by a finalize pass
+  const int mode = (k == 1 && !residual) ? kModeDirect : (k == 2 && residual) ? kModeAccum : kModeSum;
   const int S_max = (int)std::min<long long>((long long)T * k, (long long)E * C);
 
   // status word and, next to it, the fused router's arrival counter
@@ -796,6 +802,7 @@ moe_status moe_layer_forward(const void* tokens, const float* Wg, const void* W1
     a.r32 = r32;
     a.slot_w = slot_w;
     if (mode == kModeDirect) MOE_TRY(launch_zero_dropped_rows(slot_of, T, k, d, 0, out, s));
+    else if (mode == kModeSum) MOE_TRY(launch_zero_f32(static_cast<float*>(out), (size_t)T * d, s));
     else MOE_TRY(launch_zero_f32(acc32, (size_t)T * d, s));
     MOE_TRY(launch_simt_ffn1(a, rows_bound, s));
     MOE_TRY(stage_mark(4, s));

@@ -198,13 +198,33 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, int a_mn, i
   return d;
 }
 
+// GeLU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3).  Evaluated through
+// the identity 0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)), i.e. x / (1 + exp(-2u)): one exponential
+// and one division instead of a tanh, and no cancellation in 1 + tanh(u) for negative x (the
+// relative error stays at the few-ulp level of __expf and the fast division; for very negative
+// x, exp(-2u) overflows to +inf and the result is -0, the limit).
 __device__ __forceinline__ float gelu_tanh(float x) {
-  const float c = 0.7978845608028654f;  // sqrt(2/pi)
-  return 0.5f * x * (1.0f + tanhf(c * (x + 0.044715f * x * x * x)));
+  const float two_c = 1.5957691216057308f;  // 2 sqrt(2/pi)
+  const float u2 = two_c * fmaf(0.044715f * x, x * x, x);
+  return __fdividef(x, 1.0f + __expf(-u2));
 }
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// p[0..1] += v, each half rounded to nearest (subnormals kept).  Onto a zeroed output, at
+// most two addends give the same bits in either order: 0 + a is exact and a + b commutes.
+__device__ __forceinline__ void red_add_f16x2(__half* p, __half2 v) {
+  asm volatile("red.global.add.noftz.f16x2 [%0], %1;" ::"l"(p),
+               "r"(*reinterpret_cast<const uint32_t*>(&v))
+               : "memory");
+}
+
+__device__ __forceinline__ void red_add_f16(__half* p, __half v) {
+  asm volatile("red.global.add.noftz.f16 [%0], %1;" ::"l"(p),
+               "h"(*reinterpret_cast<const uint16_t*>(&v))
+               : "memory");
 }
 
 }  // namespace moe

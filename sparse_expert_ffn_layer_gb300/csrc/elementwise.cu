@@ -178,13 +178,15 @@ __global__ void splitk_reduce2_kernel(const GemmArgs g, int S_max, int T_res, in
     float v = 0.f;
     for (int ks = 0; ks < g.ksplit; ++ks) v += g.partial[((size_t)ks * g.part_rows + prow) * g.part_cols + c];
     if (res) {
-      g.r32[(size_t)row * g.ldo + c] = v;
+      if (g.mode == kModeSum) red_add_f16(g.out + (size_t)row * g.ldo + c, __float2half_rn(v));
+      else g.r32[(size_t)row * g.ldo + c] = v;
     } else if (g.mode == kModeExpertOut) {
       g.out[(size_t)row * g.ldo + c] = __float2half_rn(v);
     } else {
       const int tok = g.perm[row];
       const float w = g.slot_w[row];
       if (g.mode == kModeDirect) g.out[(size_t)tok * g.ldo + c] = __float2half_rn(w * v);
+      else if (g.mode == kModeSum) red_add_f16(g.out + (size_t)tok * g.ldo + c, __float2half_rn(w * v));
       else red_add_f32(g.acc32 + (size_t)tok * g.ldo + c, w * v);
     }
   }

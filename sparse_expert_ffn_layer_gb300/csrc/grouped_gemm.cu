@@ -344,10 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pre-work while the first tiles stream in: zero buffers the next kernel accumulates into
       const int ep_tid = blockIdx.x * 128 + (threadIdx.x - 64);
       const int ep_threads = gridDim.x * 128;
-      if (a.zero_f32) {
-        float4* z4 = reinterpret_cast<float4*>(a.zero_f32);
-        const size_t n4 = a.zero_f32_n / 4;
-        for (size_t q = ep_tid; q < n4; q += ep_threads) z4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (a.zero_buf) {
+        uint4* z4 = reinterpret_cast<uint4*>(a.zero_buf);
+        const size_t n4 = a.zero_bytes / 16;
+        for (size_t q = ep_tid; q < n4; q += ep_threads) z4[q] = make_uint4(0u, 0u, 0u, 0u);
       }
       if (a.drop_out) {
         const int gw = ep_tid >> 5, nw = ep_threads >> 5;
@@ -390,6 +390,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < t.n; c0 += 16) {
         float v[16];
         tmem_ld16(taddr + (uint32_t)c0, v);
+        if (kEpi == kEpiGeluH && ksplit == 1) {
+          // GeLU -> f16 H, two columns per 4-byte store: lanes 2i and 2i+1 hold columns m and
+          // m+1; for each pair of tokens the even lane stores token 2p of both columns and the
+          // odd lane token 2p+1, each taking the neighbour's value by one shuffle
+          __half* hbase = t.res ? a.hres_out : a.h_out;
+          const size_t ld = t.res ? (size_t)a.ldhres : (size_t)a.ldh;
+          const bool odd = lane & 1;
+#pragma unroll
+          for (int p2 = 0; p2 < 8; ++p2) {
+            const float g0 = gelu_tanh(v[2 * p2]), g1 = gelu_tanh(v[2 * p2 + 1]);
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? g0 : g1, 1);
+            const int s = c0 + 2 * p2 + (odd ? 1 : 0);
+            if (s < t.n)
+              *reinterpret_cast<__half2*>(hbase + (size_t)(t.row0 + s) * ld + (m & ~1)) =
+                  odd ? __floats2half2_rn(recv, g1) : __floats2half2_rn(g0, recv);
+          }
+          continue;
+        }
+        if (kEpi == kEpiCombine && ksplit == 1 && a.mode == kModeSum) {
+          // out += f16(w * acc), two columns per f16x2 reduction (lanes 2i, 2i+1 hold columns
+          // m, m+1; the even lane takes token 2p of both, the odd lane token 2p+1); residual
+          // rows are token rows with weight 1
+#pragma unroll
+          for (int p2 = 0; p2 < 8; ++p2) {
+            const bool odd = lane & 1;
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[2 * p2] : v[2 * p2 + 1], 1);
+            const int s = c0 + 2 * p2 + (odd ? 1 : 0);
+            if (s < t.n) {
+              const int tok = t.res ? t.row0 + s : rt[s];
+              const float w = t.res ? 1.0f : rw[s];
+              const float lo = odd ? recv : v[2 * p2], hi = odd ? v[2 * p2 + 1] : recv;
+              red_add_f16x2(a.out + (size_t)tok * a.ldo + (m & ~1), __floats2half2_rn(w * lo, w * hi));
+            }
+          }
+          continue;
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int s = c0 + j;
@@ -399,9 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int prow = t.res ? a.part_res_row0 + row : row;
             a.partial[((size_t)ks * a.part_rows + prow) * a.part_cols + m] = v[j];
           } else if (kEpi == kEpiGeluH) {
-            const __half h = __float2half_rn(gelu_tanh(v[j]));
-            if (t.res) a.hres_out[(size_t)row * a.ldhres + m] = h;
-            else a.h_out[(size_t)row * a.ldh + m] = h;
+            // (handled above)
           } else {
             if (t.res) {
               a.r32[(size_t)row * a.ldo + m] = v[j];

@@ -46,8 +46,12 @@ enum : int { kEpiGeluH = 0, kEpiCombine = 1 };
 // Output modes of the second GEMM's epilogue (expert tiles).
 enum : int {
   kModeDirect = 0,     // out[perm[s]] = f16(w_s * acc): top-1, no residual; each token once
-  kModeAccum = 1,      // acc32[perm[s]] += w_s * acc (fp32 reduction, <= 2 addends per element)
-  kModeExpertOut = 2   // out[s] = f16(acc): unscaled rows in slot order (moe_expert_ffn)
+  kModeAccum = 1,      // acc32[perm[s]] += w_s * acc, residual rows to r32, then a finalize
+                       // pass (top-2 with the residual MLP: three addends need a fixed order)
+  kModeExpertOut = 2,  // out[s] = f16(acc): unscaled rows in slot order (moe_expert_ffn)
+  kModeSum = 3         // out[perm[s]] += f16(w_s * acc), residual rows out[t] += f16(acc), into
+                       // an output zeroed before: at most two addends per element (top-2, or
+                       // one expert plus the residual MLP), so the sum is order-independent
 };
 
 struct GemmArgs {
@@ -84,8 +88,8 @@ struct GemmArgs {
   int ldo;
   const float* slot_w;      // [S] gate weight of each slot
   // first GEMM pre-work (epilogue warps, before the first tile)
-  float* zero_f32;          // buffer to clear, or null
-  size_t zero_f32_n;        // its length in floats (multiple of 4)
+  void* zero_buf;           // buffer to clear, or null
+  size_t zero_bytes;        // its length in bytes (multiple of 16)
   const int32_t* drop_slot_of;  // [T] slot of each token (top-1) for zeroing dropped rows
   int drop_T;
   __half* drop_out;         // out [T, drop_d], or null

@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs a) {
       if (res) a.Hres[(size_t)r * a.f_res + c] = h;
       else a.H[(size_t)(row0 + r) * a.f + c] = h;
     } else if (res) {
-      a.r32[(size_t)r * a.d + c] = acc[q];
+      if (a.mode == kModeSum) red_add_f32(a.out + (size_t)r * a.d + c, acc[q]);
+      else a.r32[(size_t)r * a.d + c] = acc[q];
     } else {
       const int slot = row0 + r;
       if (a.mode == kModeExpertOut) {
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs a) {
         const int tok = a.perm[slot];
         const float w = a.slot_w[slot];
         if (a.mode == kModeDirect) a.out[(size_t)tok * a.d + c] = w * acc[q];
+        else if (a.mode == kModeSum) red_add_f32(a.out + (size_t)tok * a.d + c, w * acc[q]);
         else red_add_f32(a.acc32 + (size_t)tok * a.d + c, w * acc[q]);
       }
     }
