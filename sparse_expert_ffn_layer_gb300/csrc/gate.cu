@@ -365,6 +365,105 @@ cudaError_t launch_small(const Tin* x, const float* Wg, int T, int d, int E, flo
   return go(gate_logits_small_kernel<Tin, 1>, 1, kSStages * small_slot_bytes<Tin, 1>());
 }
 
+// ---------------------------------------------------------------------------------------
+// Large batches: one warp per block computes a tile of 32 tokens x 64 experts, 8 x 8 outputs
+// per thread (tokens 4g..4g+3 and 16+4g..16+4g+3 of the tile, experts 4h..4h+3 and
+// 32+4h..32+4h+3), so each step of i takes four conflict-free 16-byte shared loads for 64
+// multiply-adds.  Wg and token chunks of 32 columns stream through a two-deep cp.async ring;
+// each chunk of token rows is widened to fp32 once (exact) into an i-major tile.  Every
+// output's chain runs in one thread in ascending i, as in the kernels above.
+constexpr int kWT = 32, kWE = 64, kWK = 32;
+
+template <typename Tin>
+struct WideSmem {
+  static constexpr int kRowBytes = kWK * (int)sizeof(Tin) + 16;   // padded: conflict-free reads
+  float ws[2][kWK][kWE];
+  uint8_t xh[2][kWT * kRowBytes];
+  float xs[kWK][kWT];
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(32) gate_logits_wide_kernel(const Tin* __restrict__ x,
+                                                              const float* __restrict__ Wg,
+                                                              int T, int d, int E,
+                                                              float* __restrict__ logits) {
+  pdl_trigger();   // the top-k kernel may start its launch; it waits for these logits
+  __shared__ __align__(16) WideSmem<Tin> sm;
+  constexpr int kRow = WideSmem<Tin>::kRowBytes;
+  constexpr int kPiece = 16 / (int)sizeof(Tin);                // values per 16-byte piece
+  constexpr int kPieces = kWK / kPiece;                        // pieces per token row chunk
+  const int lane = threadIdx.x;
+  const int t0 = blockIdx.x * kWT, e0 = blockIdx.y * kWE;
+  const int g = lane >> 3, h = lane & 7;
+  const int nch = d / kWK;
+  auto issue = [&](int c, int st) {
+    const int k0 = c * kWK;
+#pragma unroll
+    for (int q = 0; q < kWK * kWE / 4 / 32; ++q) {             // Wg: 512 pieces
+      const int idx = q * 32 + lane, row = idx >> 4, col = (idx & 15) * 4;
+      cp_async16(&sm.ws[st][row][col], Wg + (size_t)(k0 + row) * E + e0 + col, 16);
+    }
+#pragma unroll
+    for (int q = 0; q < kWT * kPieces / 32; ++q) {             // token rows
+      const int idx = q * 32 + lane, tt = idx / kPieces, pc = idx % kPieces;
+      const int t = t0 + tt;
+      cp_async16(sm.xh[st] + tt * kRow + pc * 16, x + (size_t)min(t, T - 1) * d + k0 + pc * kPiece,
+                 t < T ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+  issue(0, 0);
+  for (int c = 0; c < nch; ++c) {
+    const int st = c & 1;
+    if (c + 1 < nch) {
+      issue(c + 1, st ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncwarp();
+    {   // widen this lane's token row of the chunk into the i-major tile
+      const uint8_t* row = sm.xh[st] + lane * kRow;
+#pragma unroll
+      for (int pc = 0; pc < kPieces; ++pc) {
+        float f[kPiece];
+        unpack16(*reinterpret_cast<const uint4*>(row + pc * 16), f, static_cast<const Tin*>(nullptr));
+#pragma unroll
+        for (int v = 0; v < kPiece; ++v) sm.xs[pc * kPiece + v][lane] = f[v];
+      }
+    }
+    __syncwarp();
+#pragma unroll 4
+    for (int kk = 0; kk < kWK; ++kk) {                         // ascending i
+      const float4 xa = *reinterpret_cast<const float4*>(&sm.xs[kk][4 * g]);
+      const float4 xb = *reinterpret_cast<const float4*>(&sm.xs[kk][16 + 4 * g]);
+      const float4 wa = *reinterpret_cast<const float4*>(&sm.ws[st][kk][4 * h]);
+      const float4 wb = *reinterpret_cast<const float4*>(&sm.ws[st][kk][32 + 4 * h]);
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(xv[i], wv[j], acc[i][j]);
+    }
+    __syncwarp();                                              // chunk st may be refilled
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + (i < 4 ? 4 * g + i : 16 + 4 * g + (i - 4));
+    if (t >= T) continue;
+    float* row = logits + (size_t)t * E + e0;
+    *reinterpret_cast<float4*>(row + 4 * h) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    *reinterpret_cast<float4*>(row + 32 + 4 * h) =
+        make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+  }
+}
+
 struct PlainLoad {
   __device__ __forceinline__ float operator()(const float* p) const { return *p; }
 };
@@ -404,6 +503,23 @@ cudaError_t launch_gate_logits(const void* x, int dtype_f16, const float* Wg, in
       MOE_LAUNCH(launch_small(static_cast<const __half*>(x), Wg, T, d, E, logits, m, s));
     else
       MOE_LAUNCH(launch_small(static_cast<const float*>(x), Wg, T, d, E, logits, m, s));
+    return cudaGetLastError();
+  }
+  // The one-warp 32 x 64 tiles need several warps per SM to hide their latencies: they win
+  // from about four tiles per SM (2.4B+MoE-128 layer, T = 16384: 444 -> 360 us) and lose with
+  // fewer (350M+MoE-128, T = 4096, two tiles per SM: 44 -> 67 us).
+  const long long wide_tiles = (long long)((T + kWT - 1) / kWT) * (E / kWE);
+  const bool wide_ok = E % kWE == 0 && d % kWK == 0 && aligned &&
+                       (reinterpret_cast<uintptr_t>(logits) & 15) == 0 &&
+                       wide_tiles >= 4LL * sm_count();
+  if (wide_ok) {
+    const dim3 wg((T + kWT - 1) / kWT, E / kWE);
+    if (dtype_f16)
+      MOE_LAUNCH(launch_k(gate_logits_wide_kernel<__half>, wg, 32, 0, s, false,
+                          static_cast<const __half*>(x), Wg, T, d, E, logits));
+    else
+      MOE_LAUNCH(launch_k(gate_logits_wide_kernel<float>, wg, 32, 0, s, false,
+                          static_cast<const float*>(x), Wg, T, d, E, logits));
     return cudaGetLastError();
   }
   dim3 grid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE);

@@ -34,13 +34,19 @@ def _gate(m, tokens, Wg, k, logits_in=None):
 
 
 # ------------------------------------------------------------------------------ gate
-@pytest.mark.parametrize("name,T", [("tiny_fp32", 128), ("moe350m_e128", 1), ("moe350m_e128", 777),
-                                    ("moe1p3b_e128_zipf", 256), ("moe2p4b_e128_top2", 1024),
-                                    ("moe2p4b_e128_top2_zipf", 333), ("moe350m_e128", 2000),
-                                    ("moe350m_e128", 4100), ("prmoe_e64", 1500),
-                                    ("prmoe_e64", 2500)])
-def test_gate_bit_exact(m, name, T):
-    cfg = synth.CONFIGS[name]
+# every gate kernel the launcher picks: the lane-per-expert kernel (one and two tokens per
+# warp), the 32 x 64 warp tiles of large batches (ragged last tile), the 4 x 4 tiled kernel
+# (E not a multiple of 64) and the tiny fp32 layer
+@pytest.mark.parametrize("name,T,E", [("tiny_fp32", 128, None), ("moe350m_e128", 1, None),
+                                      ("moe350m_e128", 777, None), ("moe1p3b_e128_zipf", 256, None),
+                                      ("moe2p4b_e128_top2", 1024, None),
+                                      ("moe2p4b_e128_top2_zipf", 333, None),
+                                      ("moe350m_e128", 2000, None), ("moe350m_e128", 4100, None),
+                                      ("prmoe_e64", 1500, None), ("prmoe_e64", 2500, None),
+                                      ("moe2p4b_e128_top2", 16384, None), ("moe350m_e128", 3000, 96),
+                                      ("moe350m_e128", 3001, 36)])
+def test_gate_bit_exact(m, name, T, E):
+    cfg = synth.CONFIGS[name] if E is None else synth.CONFIGS[name].at(E=E)
     inp = synth.host_inputs(cfg, T, seed=3, with_experts=False)
     lo, pr, idx, w = _gate(m, inp["tokens"], inp["Wg"], cfg.k)
     ref_lo = oracle.gate_logits(inp["tokens"], inp["Wg"])
