@@ -143,10 +143,12 @@ __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
   __syncthreads();
 }
 
-// Split-K reduction of the first GEMM: sum the chunks in order, GeLU, round to f16.
+// Split-K reduction of the first GEMM: sum the chunks in order, GeLU, round to f16.  It lets
+// the second GEMM launch before waiting for the first: that GEMM's weight loads depend on
+// nothing this chain writes, and it waits for this kernel before it reads H.
 __global__ void splitk_reduce1_kernel(const GemmArgs g, int S_max, int T_res, int f, int f_res) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int S = g.offsets[g.E];
   const size_t n = (size_t)(S_max + T_res) * g.part_cols;
   const size_t stride = (size_t)gridDim.x * blockDim.x;

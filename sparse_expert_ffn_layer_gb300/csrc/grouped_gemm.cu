@@ -101,7 +101,10 @@ __device__ __forceinline__ Tile decode(int i, const GemmArgs& a, const int32_t* 
   return t;
 }
 
-template <bool kGatherB, int kEpi, int kMW>
+// kSplit: the decode-sized variant, whose items are cut into K chunks (fp32 partial sums,
+// summed by a reduce kernel); a template parameter so that neither variant carries the other's
+// epilogue code (at decode sizes the kernel's fixed costs decide its time).
+template <bool kGatherB, int kEpi, int kMW, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmA_res,
@@ -115,10 +118,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + a.stages;
   // TMEM accumulators form a ring of nslots slots of acc_cols columns.  Item j (the j-th
   // item of this CTA) accumulates its mw weight blocks in slots (j mw + h) mod nslots; the
-  // MMA warp waits for a slot to be drained (acc_empty[slot]) just before the first MMA into
-  // it, and the epilogue releases each slot as soon as it has read it, so the next item's
-  // MMAs overlap the epilogue whenever nslots > mw.  acc_full[j mod nslots] completes when
-  // item j's MMAs are done.
+  // MMA warp waits for the item's slots to be drained (acc_empty[slot]) before its first MMA,
+  // and the epilogue releases each slot as soon as it has read it, so the next item's MMAs
+  // overlap the epilogue whenever nslots >= 2 mw (partly when nslots > mw).
+  // acc_full[j mod nslots] completes when item j's MMAs are done.
   uint64_t* acc_full = empty + a.stages;     // [nslots]
   uint64_t* acc_empty = acc_full + kMaxSlots;  // [nslots]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc_off);
@@ -151,10 +154,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) tmem_alloc(tmem_holder, a.tmem_cols);
-  // everything above is independent of the previous kernel of the stream; from here on its
-  // results (offsets, gathered rows, H) are read and its inputs may be overwritten
-  pdl_wait();
-  pdl_trigger();
+  // Everything above is independent of the previous kernel of the stream.  With early_a the
+  // routing (offsets) comes from a kernel at least two launches back, which has completed by
+  // the time this grid starts (every kernel of the chain waits for its predecessor before it
+  // lets its successor launch), and the weights are never written: so the item list is built
+  // and the producer issues the weight loads of its first stages before the wait.
+  if (!a.early_a) {
+    pdl_wait();
+    pdl_trigger();
+  }
   // chunk prefix over experts (warp 2), E <= 1024
   if (warp == 2) {
     // offsets clamped to [0, S_bound]: offsets[E] beyond the caller's S_max cannot make a
@@ -162,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // taken as max(0, .) below); either records MOE_ERR_DEVICE_BOUNDS
     bool bad = false;
     for (int e = lane; e <= a.E; e += 32) {
-      const int o = a.offsets[e];
+      const int o = __ldcg(a.offsets + e);
       soffs[e] = min(max(o, 0), a.S_bound);
       bad |= soffs[e] != o;
     }
@@ -197,16 +205,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_exp_items = prefix[a.E] * a.mt_exp;
   const int n_res_items = a.n_res_rows > 0 ? ((a.n_res_rows + a.nmax - 1) / a.nmax) * a.mt_res : 0;
-  const int ksplit = a.ksplit;
+  const int ksplit = kSplit ? a.ksplit : 1;
   const int total = (n_exp_items + n_res_items) * ksplit;
 
   uint32_t issued = 0, issued_parity = 0;     // producer: stages with a fill in flight
+  // early_a: weight loads of the first stages, issued before the wait (their stages' token
+  // rows follow after it, in the main loop below)
+  int n_early = 0;
+  if (a.early_a && warp == 0 && lane == 0) {
+    int stage = 0;
+    for (int i = blockIdx.x; i < total && n_early < a.stages; i += gridDim.x) {
+      const Tile t = decode(i / ksplit, a, prefix, soffs);
+      const int ks = i - (i / ksplit) * ksplit;
+      const int npad = max(16, (t.n + 15) & ~15);
+      const CUtensorMap* mA = t.res ? &tmA_res : &tmA;
+      const int a_y0 = t.res ? 0 : t.e * a.a_rows_per_expert;
+      const int a_x = t.mt * mw * kBM;
+      const int nkb = t.K / kBK;
+      const int kb0 = ks * nkb / ksplit, kb1 = (ks + 1) * nkb / ksplit;
+      for (int kb = kb0; kb < kb1 && n_early < a.stages; ++kb, ++n_early, ++stage) {
+        uint8_t* sA = smem + (size_t)stage * L.stage_bytes;
+        mbar_expect_tx(&full[stage], (uint32_t)(mw * kABytes) + (uint32_t)npad * 128u);
+#pragma unroll
+        for (int h = 0; h < mw; ++h) {
+          tma_load_2d(sA + h * kABytes, mA, a_x + h * kBM, a_y0 + kb * kBK, &full[stage]);
+          tma_load_2d(sA + h * kABytes + kABytes / 2, mA, a_x + h * kBM + 64, a_y0 + kb * kBK,
+                      &full[stage]);
+        }
+        issued |= 1u << stage;                   // phase 0 of a fresh stage
+      }
+    }
+  }
+  if (a.early_a) {
+    pdl_wait();
+    pdl_trigger();
+  }
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0;
+    n_early = __shfl_sync(0xffffffffu, n_early, 0);
+    int it = 0;                                   // k-iterations so far (the first n_early
+                                                  // have their weight loads in flight)
+    bool bad_row = false;
     // this lane's gather rows (first GEMM): groups g = lane, lane + 32 of four rows each;
-    // the next tile's rows are fetched while the current tile streams
+    // the next tile's rows are fetched while the current tile streams.  A perm entry outside
+    // [0, T) is replaced by row 0 and reported once at the end.
     auto load_rows = [&](const Tile& t, int (&rows)[2][4]) {
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -214,12 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) {
           const int r = 4 * (lane + 32 * h) + q;
           const int src = t.row0 + (r < t.n ? r : 0);
-          int tok = t.res ? src : a.perm[src];
-          if ((unsigned)tok >= (unsigned)a.n_tokens) {   // not a token of this batch
-            record_status(a.status, kErrBounds);
-            tok = 0;
-          }
-          rows[h][q] = tok;
+          const int tok = t.res ? src : a.perm[src];
+          const bool oob = (unsigned)tok >= (unsigned)a.n_tokens;
+          bad_row |= oob;
+          rows[h][q] = oob ? 0 : tok;
         }
     };
     int rows[2][4], rows_next[2][4];
@@ -236,24 +278,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_rows(decode((i + gridDim.x) / ksplit, a, prefix, soffs), rows_next);
       const int nkb = t.K / kBK;
       const int kb0 = ks * nkb / ksplit, kb1 = (ks + 1) * nkb / ksplit;
-      for (int kb = kb0; kb < kb1; ++kb) {
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, a.wait_ns);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
         uint8_t* sA = smem + (size_t)stage * L.stage_bytes;
         uint8_t* sB = sA + L.b_off;
-        if (lane == 0) {
-          mbar_expect_tx(&full[stage], (uint32_t)(mw * kABytes) + (uint32_t)npad * 128u);
-        }
-        __syncwarp();
-        if (lane == 0) {
+        if (it >= n_early) {                          // else: weights already in flight
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, a.wait_ns);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_expect_tx(&full[stage], (uint32_t)(mw * kABytes) + (uint32_t)npad * 128u);
 #pragma unroll
-          for (int h = 0; h < mw; ++h) {               // mw adjacent 128-row blocks
-            tma_load_2d(sA + h * kABytes, mA, a_x + h * kBM, a_y0 + kb * kBK, &full[stage]);
-            tma_load_2d(sA + h * kABytes + kABytes / 2, mA, a_x + h * kBM + 64, a_y0 + kb * kBK,
-                        &full[stage]);
+            for (int h = 0; h < mw; ++h) {               // mw adjacent 128-row blocks
+              tma_load_2d(sA + h * kABytes, mA, a_x + h * kBM, a_y0 + kb * kBK, &full[stage]);
+              tma_load_2d(sA + h * kABytes + kABytes / 2, mA, a_x + h * kBM + 64, a_y0 + kb * kBK,
+                          &full[stage]);
+            }
           }
+          __syncwarp();
         }
         if (kGatherB) {
 #pragma unroll
@@ -281,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 4; ++q) rows[h][q] = rows_next[h][q];
       }
     }
+    if (kGatherB && __any_sync(0xffffffffu, bad_row) && lane == 0) record_status(a.status, kErrBounds);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     int stage = 0;
@@ -294,7 +337,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t d_tmem[mw];
 #pragma unroll
       for (int h = 0; h < mw; ++h) d_tmem[h] = tmem_base + ((blk0 + h) % a.nslots) * a.acc_cols;
+      // the item's accumulator slots must have been drained by the epilogue
       bool ok = true;
+      if (lane == 0) {
+        for (int h = 0; h < mw && ok; ++h) {
+          const uint32_t blk = blk0 + h;
+          ok = mbar_wait_bounded(&acc_empty[blk % a.nslots], ((blk / a.nslots) & 1u) ^ 1u,
+                                 abort_flag, a.status, a.wait_ns);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
       const uint32_t idesc = idesc_f16(kBM, npad, 1, 0);
       const int nkb = t.K / kBK;
       const int kb0 = ks * nkb / ksplit, kb1 = (ks + 1) * nkb / ksplit;
@@ -311,22 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
 #pragma unroll
             for (int h = 0; h < mw; ++h) {             // same token rows, mw weight blocks
-              if (kb == kb0 && kk == 0 && ok) {
-                // first MMA into this block: its slot must have been drained by the epilogue
-                const uint32_t blk = blk0 + h;
-                ok = mbar_wait_bounded(&acc_empty[blk % a.nslots], ((blk / a.nslots) & 1u) ^ 1u,
-                                       abort_flag, a.status, a.wait_ns);
-                tc_fence_after();
-              }
-              if (!ok) break;
               const uint64_t ad = smem_desc(a0 + h * kABytes + kk * 2048, a.a_lbo, a.a_sbo, 2);
               tc_mma_f16(d_tmem[h], ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
             }
           }
-          if (ok) tc_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          tc_commit(&empty[stage]);        // frees the stage once these MMAs have read it
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+        __syncwarp();
         if (++stage == a.stages) {
           stage = 0;
           phase ^= 1u;
@@ -365,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // second GEMM: each warp stages the tile's tokens and gate weights in its own shared
       // memory while the accumulator is still being computed (a load per row per warp
       // instead of one per row per thread; warp-private, so no cross-warp barrier)
-      const bool scatter = kEpi == kEpiCombine && !t.res && a.mode != kModeExpertOut && ksplit == 1;
+      const bool scatter = kEpi == kEpiCombine && !t.res && a.mode != kModeExpertOut && !kSplit;
       int32_t* rt = row_tok + quarter * a.nmax;
       float* rw = row_w + quarter * a.nmax;
       if (scatter) {
@@ -390,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < t.n; c0 += 16) {
         float v[16];
         tmem_ld16(taddr + (uint32_t)c0, v);
-        if (kEpi == kEpiGeluH && ksplit == 1) {
+        if (kEpi == kEpiGeluH && !kSplit) {
           // GeLU -> f16 H, two columns per 4-byte store: lanes 2i and 2i+1 hold columns m and
           // m+1; for each pair of tokens the even lane stores token 2p of both columns and the
           // odd lane token 2p+1, each taking the neighbour's value by one shuffle
@@ -408,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           continue;
         }
-        if (kEpi == kEpiCombine && ksplit == 1 && a.mode == kModeSum) {
+        if (kEpi == kEpiCombine && !kSplit && a.mode == kModeSum) {
           // out += f16(w * acc), two columns per f16x2 reduction (lanes 2i, 2i+1 hold columns
           // m, m+1; the even lane takes token 2p of both, the odd lane token 2p+1); residual
           // rows are token rows with weight 1
@@ -431,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = c0 + j;
           if (s >= t.n) break;
           const int row = t.row0 + s;
-          if (ksplit > 1) {
+          if (kSplit) {
             const int prow = t.res ? a.part_res_row0 + row : row;
             a.partial[((size_t)ks * a.part_rows + prow) * a.part_cols + m] = v[j];
           } else if (kEpi == kEpiGeluH) {
@@ -481,27 +526,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTA of the previous GEMM on the same SM.
 constexpr size_t kMinGemmSmem = 116 * 1024;
 
-template <bool G, int Epi, int MW>
+template <bool G, int Epi, int MW, bool Split>
 cudaError_t launch_mw(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                       const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s,
                       bool pdl) {
   const SmemLayout L = smem_layout(args.nmax, args.stages, args.E, MW);
-  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_kernel<G, Epi, MW>));
+  auto kern = grouped_gemm_kernel<G, Epi, MW, Split>;
+  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern));
   if (err != cudaSuccess) return err;
-  return launch_k(grouped_gemm_kernel<G, Epi, MW>, grid, kThreads,
-                  std::max<size_t>(L.total, kMinGemmSmem), s, pdl, A, B, Ar, Br, args);
+  return launch_k(kern, grid, kThreads, std::max<size_t>(L.total, kMinGemmSmem), s, pdl, A, B, Ar,
+                  Br, args);
+}
+
+template <bool G, int Epi, bool Split>
+cudaError_t launch_split(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
+                         const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s,
+                         bool pdl) {
+  switch (args.mw) {
+    case 1: return launch_mw<G, Epi, 1, Split>(A, B, Ar, Br, args, grid, s, pdl);
+    case 2: return launch_mw<G, Epi, 2, Split>(A, B, Ar, Br, args, grid, s, pdl);
+    case 4: return launch_mw<G, Epi, 4, Split>(A, B, Ar, Br, args, grid, s, pdl);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <bool G, int Epi>
 cudaError_t launch_one(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                        const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s,
                        bool pdl) {
-  switch (args.mw) {
-    case 1: return launch_mw<G, Epi, 1>(A, B, Ar, Br, args, grid, s, pdl);
-    case 2: return launch_mw<G, Epi, 2>(A, B, Ar, Br, args, grid, s, pdl);
-    case 4: return launch_mw<G, Epi, 4>(A, B, Ar, Br, args, grid, s, pdl);
-  }
-  return cudaErrorInvalidValue;
+  return args.ksplit > 1 ? launch_split<G, Epi, true>(A, B, Ar, Br, args, grid, s, pdl)
+                         : launch_split<G, Epi, false>(A, B, Ar, Br, args, grid, s, pdl);
 }
 
 }  // namespace

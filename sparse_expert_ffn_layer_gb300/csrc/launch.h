@@ -101,6 +101,9 @@ struct GemmArgs {
   int ksplit;
   float* partial;
   int part_rows, part_cols, part_res_row0;
+  // 1: the offsets come from a kernel at least two launches back (the weights of the first
+  // stages are loaded before the wait on the previous kernel)
+  int early_a;
   // error reporting
   int* status;
   uint64_t wait_ns;
