@@ -505,6 +505,23 @@ def run_ours(args):
     torch.cuda.synchronize()
     ms_e2e = h0.elapsed_time(h1)
 
+    # the box's plain pinned copy rates for this step's buffers (one cudaMemcpyAsync per copy,
+    # CUDA events on a copy stream), beside the end-to-end number they bound
+    def copy_gbs(dst, src, reps=10):
+        cs = torch.cuda.Stream()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cs):
+            dst.copy_(src, non_blocking=True)
+            c0.record(cs)
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+            c1.record(cs)
+        torch.cuda.synchronize()
+        return reps * src.numel() * src.element_size() / (c0.elapsed_time(c1) / 1000.0) / 1e9
+
+    h2d_gbs = copy_gbs(dev_in[0], host_tok[0])
+    d2h_gbs = copy_gbs(host_outs[0], dev_out[0])
+
     if world > 1:
         ms, ms_e2e = max_over_ranks([ms, ms_e2e], dist, "cuda")
     if rank != 0:
@@ -568,7 +585,8 @@ def run_ours(args):
         "routing": {"active_experts": A, "kept_slots": S},
         "e2e": {"value": value_e2e, "unit": UNIT, "h2d_bytes_per_step": T * cfg.d * el,
                 "d2h_bytes_per_step": T * cfg.d * el,
-                "mode": "pinned host copies in and out every step, two-deep pipeline with compute"},
+                "mode": "pinned host copies in and out every step, two-deep pipeline with compute",
+                "copy_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}},
         "gpu_launches": K * launches_per_step,
         "launch": "direct" if args.no_graph else "one CUDA graph per step, replayed back to back",
         "clocks": clocks.summary(t_wall0, t_wall1),

@@ -80,10 +80,13 @@ __global__ void finalize_kernel(const float* __restrict__ acc32, const float* __
 }
 
 // out[t] = sum_j [slot >= 0] w_j expert_out[slot] (+ residual_in[t]); one warp per token row.
-template <typename T_>
+// Each lane handles V consecutive columns with 16-byte accesses (V = 8 halves or 4 floats;
+// V = 1 where the row length does not allow it).
+template <typename T_, int V>
 __global__ void combine_kernel(const T_* __restrict__ eo, const int32_t* __restrict__ slot_of,
                                const float* __restrict__ topk_w, const T_* __restrict__ res,
                                int T, int d, int k, T_* __restrict__ out) {
+  struct alignas(V * sizeof(T_)) Vec { T_ v[V]; };
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
@@ -93,12 +96,25 @@ __global__ void combine_kernel(const T_* __restrict__ eo, const int32_t* __restr
       s[j] = slot_of[(size_t)t * k + j];
       w[j] = topk_w[(size_t)t * k + j];
     }
-    for (int c = lane; c < d; c += 32) {
-      float acc = 0.f;
-      for (int j = 0; j < k; ++j)
-        if (s[j] >= 0) acc += w[j] * as_f32<T_>(eo[(size_t)s[j] * d + c]);
-      if (res) acc += as_f32<T_>(res[(size_t)t * d + c]);
-      out[(size_t)t * d + c] = from_f32<T_>(acc);
+    for (int c = lane * V; c < d; c += 32 * V) {
+      float acc[V];
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        if (s[j] < 0) continue;
+        const Vec e = *reinterpret_cast<const Vec*>(eo + (size_t)s[j] * d + c);
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] += w[j] * as_f32<T_>(e.v[q]);
+      }
+      if (res) {
+        const Vec r = *reinterpret_cast<const Vec*>(res + (size_t)t * d + c);
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] += as_f32<T_>(r.v[q]);
+      }
+      Vec o;
+#pragma unroll
+      for (int q = 0; q < V; ++q) o.v[q] = from_f32<T_>(acc[q]);
+      *reinterpret_cast<Vec*>(out + (size_t)t * d + c) = o;
     }
   }
 }
@@ -245,15 +261,29 @@ cudaError_t launch_combine(const void* expert_out, const int32_t* slot_of, const
                            const void* residual_in, int dtype_f16, int T, int d, int k, void* out,
                            cudaStream_t s) {
   const int g = grid_for((size_t)T * 32, 256);
-  if (dtype_f16)
-    MOE_LAUNCH(launch_k(combine_kernel<__half>, g, 256, 0, s, false,
-                        static_cast<const __half*>(expert_out), slot_of, topk_w,
-                        static_cast<const __half*>(residual_in), T, d, k,
-                        static_cast<__half*>(out)));
-  else
-    MOE_LAUNCH(launch_k(combine_kernel<float>, g, 256, 0, s, false,
-                        static_cast<const float*>(expert_out), slot_of, topk_w,
-                        static_cast<const float*>(residual_in), T, d, k, static_cast<float*>(out)));
+  const bool a16 = ((reinterpret_cast<uintptr_t>(expert_out) | reinterpret_cast<uintptr_t>(out) |
+                     reinterpret_cast<uintptr_t>(residual_in)) & 15) == 0;
+  if (dtype_f16) {
+    const __half* eo = static_cast<const __half*>(expert_out);
+    const __half* ri = static_cast<const __half*>(residual_in);
+    __half* o = static_cast<__half*>(out);
+    if (d % 8 == 0 && a16)
+      MOE_LAUNCH(launch_k(combine_kernel<__half, 8>, g, 256, 0, s, false, eo, slot_of, topk_w, ri, T,
+                          d, k, o));
+    else
+      MOE_LAUNCH(launch_k(combine_kernel<__half, 1>, g, 256, 0, s, false, eo, slot_of, topk_w, ri, T,
+                          d, k, o));
+  } else {
+    const float* eo = static_cast<const float*>(expert_out);
+    const float* ri = static_cast<const float*>(residual_in);
+    float* o = static_cast<float*>(out);
+    if (d % 4 == 0 && a16)
+      MOE_LAUNCH(launch_k(combine_kernel<float, 4>, g, 256, 0, s, false, eo, slot_of, topk_w, ri, T,
+                          d, k, o));
+    else
+      MOE_LAUNCH(launch_k(combine_kernel<float, 1>, g, 256, 0, s, false, eo, slot_of, topk_w, ri, T,
+                          d, k, o));
+  }
   return cudaGetLastError();
 }
 

@@ -14,7 +14,8 @@
 // E / 8 CTAs (16 at E = 128) pull Wg in parallel.  The last CTA to finish (a counter in the
 // workspace, cleared by the caller before the launch and by that CTA after use) then routes
 // the whole batch: a warp per token for softmax / top-k, then the dispatch of the T * k <= 128
-// assignments by one block (rank = earlier assignments to the same expert, counted directly).
+// assignments by one block (per-expert counts and ranks counted directly over the assignment
+// list, no atomics).
 #include "launch.h"
 #include "topk.cuh"
 
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kRThreads) gate_route_small_kernel(const Route
   int32_t* s_cnt = reinterpret_cast<int32_t*>(s_w + 128);   // [E]
   int32_t* s_off = s_cnt + a.E;                             // [E]
   int32_t* s_wsum = s_off + a.E;                            // [kWarps]
-  for (int e = threadIdx.x; e < a.E; e += kRThreads) s_cnt[e] = 0;
+
   for (int tok = w; tok < a.T; tok += kWarps) {
     const TopK r = softmax_topk_warp(a.logits + (size_t)tok * a.E, a.E, a.k, lane, L2Load(),
                                      nullptr, nullptr);
@@ -154,8 +155,13 @@ __global__ void __launch_bounds__(kRThreads) gate_route_small_kernel(const Route
     }
   }
   __syncthreads();
-  for (int q = threadIdx.x; q < n; q += kRThreads)   // (NaN logits give no valid expert)
-    if ((unsigned)s_idx[q] < (unsigned)a.E) atomicAdd(&s_cnt[s_idx[q]], 1);
+  // assignments per expert, counted directly over the <= 128 assignments (no atomics; an index
+  // outside [0, E) from NaN logits matches no expert)
+  for (int e = threadIdx.x; e < a.E; e += kRThreads) {
+    int c = 0;
+    for (int q = 0; q < n; ++q) c += s_idx[q] == e;
+    s_cnt[e] = c;
+  }
   __syncthreads();
   // kept = min(count, C) and its exclusive scan; thread th owns a run of experts
   const int per = (a.E + kRThreads - 1) / kRThreads;
