@@ -13,12 +13,13 @@
 // Inference review, "제안 방법").  So each (expert, M-tile) weight tile is read once, by one
 // CTA, through a deep TMA pipeline, while the token rows come from L2.
 //
-// Kernel shape: persistent, one CTA per SM, 6 warps.
+// Kernel shape: persistent, one CTA per SM.
 //   warp 0      producer: TMA of the A tile (two 64-wide boxes, 128-byte swizzle) and of the
-//               B rows (tile::gather4 through perm for GEMM1, 16-row boxes for GEMM2)
+//               B rows (tile::gather4 through perm, or 16-row boxes of contiguous rows)
 //   warp 1      TMEM allocation and the MMA issue (one elected lane)
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, GeLU / gate-weighted combine,
-//               stores; TMEM double-buffered so the epilogue of tile i overlaps tile i+1.
+//   warps 2..   epilogue (eight warps, four in the decode-sized variant): tcgen05.ld of the
+//               fp32 accumulator, GeLU / gate-weighted combine, stores; TMEM accumulators in a
+//               ring of slots so the epilogue of one item overlaps the next item's MMAs.
 // Work items are (tile of <= nmax rows of one group, M-tile), groups being the experts in
 // slot order plus, for the residual variant, one group of all T tokens using the dense MLP
 // weights (PR-MoE's fixed MLP, DeepSpeed-MoE review "Phenomenon2": Residual-MoE).
@@ -30,7 +31,16 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 192;
+// Warps: producer, MMA, then the epilogue warps: eight (two per TMEM lane quarter, taking
+// alternate 16-column chunks) for full-size items, so that an item's accumulator slots drain
+// in half the time and the next item's MMAs wait less (with 160-row tiles only three slots
+// fit TMEM; first GEMM of the 2.4B top-2 layer at T = 16384: 2390 -> 2327 us with eight
+// instead of four); four for the decode-sized variant, whose items are a few columns wide.
+template <bool kSplit>
+struct Roles {
+  static constexpr int kEpiWarps = kSplit ? 4 : 8;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+};
 constexpr int kBM = 128;          // MMA M (weight rows per accumulator)
 constexpr int kBK = 64;           // K per pipeline stage (one 128-byte swizzle span of f16)
 constexpr int kABytes = kBM * kBK * 2;   // one 128-row A block per stage; an item has mw of them
@@ -40,7 +50,8 @@ struct SmemLayout {
   uint32_t stage_bytes, b_off, bars_off, misc_off, rows_off, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int nmax, int stages, int E, int mw) {
+__host__ __device__ inline SmemLayout smem_layout(int nmax, int stages, int E, int mw,
+                                                  int epi_warps) {
   SmemLayout L;
   L.b_off = (uint32_t)mw * kABytes;
   L.stage_bytes = L.b_off + (uint32_t)nmax * 128u;
@@ -50,7 +61,8 @@ __host__ __device__ inline SmemLayout smem_layout(int nmax, int stages, int E, i
   L.misc_off = off;
   off += 16u + 8u * (uint32_t)(E + 1);       // tmem base, abort flag, chunk prefix, offsets
   L.rows_off = off;
-  off += 4u * 2u * 4u * (uint32_t)nmax;      // epilogue: per warp [nmax] tokens and gate weights
+  off += (uint32_t)epi_warps * 2u * 4u * (uint32_t)nmax;  // per epilogue warp [nmax] tokens
+                                                          // and gate weights
   L.total = off + 1024u;                     // slack for 1024-byte alignment
   return L;
 }
@@ -105,14 +117,16 @@ __device__ __forceinline__ Tile decode(int i, const GemmArgs& a, const int32_t* 
 // summed by a reduce kernel); a template parameter so that neither variant carries the other's
 // epilogue code (at decode sizes the kernel's fixed costs decide its time).
 template <bool kGatherB, int kEpi, int kMW, bool kSplit>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmA_res,
                         const __grid_constant__ CUtensorMap tmB_res, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = smem_layout(a.nmax, a.stages, a.E, a.mw);
+  constexpr int kEpiWarps = Roles<kSplit>::kEpiWarps;
+  constexpr int kEpiThreads = 32 * kEpiWarps;
+  const SmemLayout L = smem_layout(a.nmax, a.stages, a.E, a.mw, kEpiWarps);
   constexpr int mw = kMW;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off);
   uint64_t* empty = full + a.stages;
@@ -128,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.misc_off + 16);
   int32_t* soffs = prefix + (a.E + 1);                     // copy of offsets[0 .. E]
-  int32_t* row_tok = reinterpret_cast<int32_t*>(smem + L.rows_off);   // [4 warps][nmax]
-  float* row_w = reinterpret_cast<float*>(row_tok + 4 * a.nmax);      // [4 warps][nmax]
+  int32_t* row_tok = reinterpret_cast<int32_t*>(smem + L.rows_off);   // [epilogue warps][nmax]
+  float* row_w = reinterpret_cast<float*>(row_tok + kEpiWarps * a.nmax);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -140,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < a.nslots; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 128);
+      mbar_init(&acc_empty[b], kEpiThreads);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -382,13 +396,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (warps 2..)
     const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
-    const int row_in_tile = 32 * quarter + lane;
+    const int half = (warp - 2) >> 2;              // which 16-column chunks: c0 / 16 = half mod
+    const int row_in_tile = 32 * quarter + lane;   // (epilogue warps / 4)
     if (kEpi == kEpiGeluH) {
       // pre-work while the first tiles stream in: zero buffers the next kernel accumulates into
-      const int ep_tid = blockIdx.x * 128 + (threadIdx.x - 64);
-      const int ep_threads = gridDim.x * 128;
+      const int ep_tid = blockIdx.x * kEpiThreads + (threadIdx.x - 64);
+      const int ep_threads = gridDim.x * kEpiThreads;
       if (a.zero_buf) {
         uint4* z4 = reinterpret_cast<uint4*>(a.zero_buf);
         const size_t n4 = a.zero_bytes / 16;
@@ -411,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // memory while the accumulator is still being computed (a load per row per warp
       // instead of one per row per thread; warp-private, so no cross-warp barrier)
       const bool scatter = kEpi == kEpiCombine && !t.res && a.mode != kModeExpertOut && !kSplit;
-      int32_t* rt = row_tok + quarter * a.nmax;
-      float* rw = row_w + quarter * a.nmax;
+      int32_t* rt = row_tok + (warp - 2) * a.nmax;
+      float* rw = row_w + (warp - 2) * a.nmax;
       if (scatter) {
         for (int r = lane; r < t.n; r += 32) {
           rt[r] = a.perm[t.row0 + r];
@@ -432,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = (t.mt * mw + h) * kBM + row_in_tile;
       const uint32_t slot = ((uint32_t)local * mw + h) % a.nslots;
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16) + slot * a.acc_cols;
-      for (int c0 = 0; c0 < t.n; c0 += 16) {
+      for (int c0 = 16 * half; c0 < t.n; c0 += 16 * (kEpiWarps / 4)) {
         float v[16];
         tmem_ld16(taddr + (uint32_t)c0, v);
         if (kEpi == kEpiGeluH && !kSplit) {
@@ -530,12 +545,12 @@ template <bool G, int Epi, int MW, bool Split>
 cudaError_t launch_mw(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Ar,
                       const CUtensorMap& Br, const GemmArgs& args, int grid, cudaStream_t s,
                       bool pdl) {
-  const SmemLayout L = smem_layout(args.nmax, args.stages, args.E, MW);
+  const SmemLayout L = smem_layout(args.nmax, args.stages, args.E, MW, Roles<Split>::kEpiWarps);
   auto kern = grouped_gemm_kernel<G, Epi, MW, Split>;
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern));
   if (err != cudaSuccess) return err;
-  return launch_k(kern, grid, kThreads, std::max<size_t>(L.total, kMinGemmSmem), s, pdl, A, B, Ar,
-                  Br, args);
+  return launch_k(kern, grid, Roles<Split>::kThreads, std::max<size_t>(L.total, kMinGemmSmem), s,
+                  pdl, A, B, Ar, Br, args);
 }
 
 template <bool G, int Epi, bool Split>
@@ -561,8 +576,9 @@ cudaError_t launch_one(const CUtensorMap& A, const CUtensorMap& B, const CUtenso
 }  // namespace
 
 int gemm_stages_for(int nmax, int E, int mw, int smem_limit) {
+  // the larger (full-size) epilogue's staging, so that the count holds for either variant
   for (int st = 8; st >= 2; --st)
-    if ((int)smem_layout(nmax, st, E, mw).total <= smem_limit) return st;
+    if ((int)smem_layout(nmax, st, E, mw, Roles<false>::kEpiWarps).total <= smem_limit) return st;
   return 0;
 }
 
