@@ -229,6 +229,29 @@ def test_layer_forward_capacity_and_residual(m, name, T, cf):
     torch.cuda.empty_cache()
 
 
+# Output modes that no configured layer reaches, every row: top-2 with the residual MLP (three
+# addends per output: fp32 accumulators and the finalize pass), through the split-K decode path
+# and the full-size path; the fp32 layer with top-2, with the residual MLP, and with both
+# (the CUDA-core path's in-place sums and fp32 accumulators)
+@pytest.mark.parametrize("name,T,over", [
+    ("prmoe_e64", 16, {"k": 2}), ("prmoe_e64", 200, {"k": 2}),
+    ("tiny_fp32", 96, {"k": 2}), ("tiny_fp32", 96, {"residual": True, "f_res": 128}),
+    ("tiny_fp32", 96, {"k": 2, "residual": True, "f_res": 192})])
+def test_layer_output_modes(m, name, T, over):
+    cfg = synth.CONFIGS[name].at(**over)
+    case = Case(cfg, T, seed=12)
+    out, idx, slot = case.forward(m)
+    r = case.routing()
+    assert np.array_equal(idx, r.topk_idx) and np.array_equal(slot, r.disp.slot_of)
+    rows = np.arange(T, dtype=np.int32)
+    ok, err, bound = within_tol(out[rows], case.reference_rows(rows))
+    assert ok, f"max err {err:.3e} > bound {bound:.3e}"
+    b, _, _ = case.forward(m)
+    assert np.array_equal(out.view(np.uint32), b.view(np.uint32))     # deterministic
+    del case
+    torch.cuda.empty_cache()
+
+
 def test_layer_350m_every_row(m):
     """350M+MoE-128 layer, T = 4096, top-1, cf 1.25: every row against the oracle."""
     cfg = synth.CONFIGS["moe350m_e128"]
