@@ -419,48 +419,8 @@ def run_ours(args):
         raise RuntimeError(f"device status {moe.moe_status_string(status)}")
     ms = e0.elapsed_time(e1)
 
-    # decode sizes: the same steps with warm weights (one batch's graph replayed, so its
-    # routed experts' weights stay in L2 from one step to the next), beside the cold number
-    warm = None
-    if plain and T <= 64 and world == 1:
-        for _ in range(3):
-            plain[0].replay()
-        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        w0.record(stream)
-        for _ in range(K):
-            plain[0].replay()
-        w1.record(stream)
-        torch.cuda.synchronize()
-        wms = w0.elapsed_time(w1)
-        warm = {"value": job_tokens_per_s(1, T, K, wms), "unit": UNIT, "ms_per_step": wms / K,
-                "active_experts": stats[0][0],
-                "mode": "one token batch replayed K times: its routed experts' weights stay in L2"}
-
-    # stage pass: the same K steps, each with its own stage events
-    if args.no_graph:
-        for i in range(K):
-            moe.moe_set_stage_events(evs[i])
-            step(dev_tok[i % n_batches])
-        moe.moe_set_stage_events(None)
-        stage_source = "second pass of K direct calls with stage events"
-    else:
-        staged = [capture(i % n_batches, evs[i]) for i in range(K)]
-        torch.cuda.synchronize()
-        for g in staged:
-            g.replay()
-        stage_source = "second pass of K graph replays with stage events"
-    torch.cuda.synchronize()
-    stage_ms = np.zeros(moe.MOE_STAGE_EVENTS - 1)
-    for i in range(K):
-        for j in range(moe.MOE_STAGE_EVENTS - 1):
-            stage_ms[j] += evs[i][j].elapsed_time(evs[i][j + 1])
-    stage_ms /= K
-    # spread of single steps (first to last stage event of each staged step; each includes
-    # the event records, so it sits a little above the event-free mean)
-    step_each = np.array([evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)])
-    step_pct = {f"p{q}": float(np.percentile(step_each, q)) for q in (10, 50, 90)}
-
-    # end to end through the public API with host buffers: every step copies its tokens from
+    # End to end through the public API with host buffers, right after the timed pass (the same
+    # thermal and power state): every step copies its tokens from
     # pinned host memory to the device, runs the layer and copies its output back.  Two-deep
     # pipeline as a serving loop runs it: step i+1's tokens go in and step i's output comes out
     # on copy streams while step i+1 computes (double-buffered device input and output).
@@ -515,6 +475,47 @@ def run_ours(args):
     h1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = h0.elapsed_time(h1)
+
+    # decode sizes: the same steps with warm weights (one batch's graph replayed, so its
+    # routed experts' weights stay in L2 from one step to the next), beside the cold number
+    warm = None
+    if plain and T <= 64 and world == 1:
+        for _ in range(3):
+            plain[0].replay()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        for _ in range(K):
+            plain[0].replay()
+        w1.record(stream)
+        torch.cuda.synchronize()
+        wms = w0.elapsed_time(w1)
+        warm = {"value": job_tokens_per_s(1, T, K, wms), "unit": UNIT, "ms_per_step": wms / K,
+                "active_experts": stats[0][0],
+                "mode": "one token batch replayed K times: its routed experts' weights stay in L2"}
+
+    # stage pass: the same K steps, each with its own stage events
+    if args.no_graph:
+        for i in range(K):
+            moe.moe_set_stage_events(evs[i])
+            step(dev_tok[i % n_batches])
+        moe.moe_set_stage_events(None)
+        stage_source = "second pass of K direct calls with stage events"
+    else:
+        staged = [capture(i % n_batches, evs[i]) for i in range(K)]
+        torch.cuda.synchronize()
+        for g in staged:
+            g.replay()
+        stage_source = "second pass of K graph replays with stage events"
+    torch.cuda.synchronize()
+    stage_ms = np.zeros(moe.MOE_STAGE_EVENTS - 1)
+    for i in range(K):
+        for j in range(moe.MOE_STAGE_EVENTS - 1):
+            stage_ms[j] += evs[i][j].elapsed_time(evs[i][j + 1])
+    stage_ms /= K
+    # spread of single steps (first to last stage event of each staged step; each includes
+    # the event records, so it sits a little above the event-free mean)
+    step_each = np.array([evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)])
+    step_pct = {f"p{q}": float(np.percentile(step_each, q)) for q in (10, 50, 90)}
 
     # the box's plain pinned copy rates for this step's buffers (one cudaMemcpyAsync per copy,
     # CUDA events on a copy stream), beside the end-to-end number they bound
