@@ -221,10 +221,4 @@ __device__ __forceinline__ void red_add_f16x2(__half* p, __half2 v) {
                : "memory");
 }
 
-__device__ __forceinline__ void red_add_f16(__half* p, __half v) {
-  asm volatile("red.global.add.noftz.f16 [%0], %1;" ::"l"(p),
-               "h"(*reinterpret_cast<const uint16_t*>(&v))
-               : "memory");
-}
-
 }  // namespace moe

@@ -181,31 +181,80 @@ __global__ void splitk_reduce1_kernel(const GemmArgs g, int S_max, int T_res, in
   }
 }
 
-// Split-K reduction of the second GEMM: sum the chunks in order, then the combine.
+// Split-K reduction of the second GEMM, then the combine.  Four threads (a quad of lanes)
+// share four adjacent columns of one partial row: thread p sums chunks p, p + 4, p + 8, ... in
+// ascending order with 16-byte loads, all independent, so many are in flight at once; the quad
+// then adds (s0 + s1) + (s2 + s3) (each pair added in the same order by both lanes that form
+// it), so every run gives the same bits.
 __global__ void splitk_reduce2_kernel(const GemmArgs g, int S_max, int T_res, int d) {
   pdl_wait();
   pdl_trigger();
-  const int S = g.offsets[g.E];
-  const size_t n = (size_t)(S_max + T_res) * d;
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += stride) {
-    const int prow = (int)(q / d), c = (int)(q % d);
+  const int S = min(max(g.offsets[g.E], 0), S_max);
+  const int cols4 = d / 4;
+  const size_t n = (size_t)(S_max + T_res) * cols4;
+  const int p = threadIdx.x & 3;
+  // a warp takes eight quads per step; the loop bound is the same for the whole warp, so every
+  // shuffle below has all 32 lanes
+  const size_t gw = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const size_t nw = (size_t)gridDim.x * blockDim.x / 32;
+  for (size_t qb = gw * 8; qb < n; qb += nw * 8) {
+    const size_t q = qb + (threadIdx.x & 31) / 4;
+    const int prow = (int)(q / cols4), c = (int)(q % cols4) * 4;
     const bool res = prow >= S_max;
     const int row = res ? prow - S_max : prow;
-    if (!res && row >= S) continue;
-    float v = 0.f;
-    for (int ks = 0; ks < g.ksplit; ++ks) v += g.partial[((size_t)ks * g.part_rows + prow) * g.part_cols + c];
+    const bool live = q < n && (res || row < S);
+    const int nks = g.ksplit;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) {
+      const float* base = g.partial + (size_t)prow * g.part_cols + c;
+      const size_t ks_stride = (size_t)g.part_rows * g.part_cols;
+#pragma unroll 4
+      for (int ks = p; ks < nks; ks += 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(base + (size_t)ks * ks_stride));
+        v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+      }
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+      v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+      v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+      v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
+    }
+    if (!live || p != 0) continue;
     if (res) {
-      if (g.mode == kModeSum) red_add_f16(g.out + (size_t)row * g.ldo + c, __float2half_rn(v));
-      else g.r32[(size_t)row * g.ldo + c] = v;
+      __half* o = g.out + (size_t)row * g.ldo + c;
+      if (g.mode == kModeSum) {
+        red_add_f16x2(o, __floats2half2_rn(v.x, v.y));
+        red_add_f16x2(o + 2, __floats2half2_rn(v.z, v.w));
+      } else {
+        *reinterpret_cast<float4*>(g.r32 + (size_t)row * g.ldo + c) = v;
+      }
     } else if (g.mode == kModeExpertOut) {
-      g.out[(size_t)row * g.ldo + c] = __float2half_rn(v);
+      __half2* o = reinterpret_cast<__half2*>(g.out + (size_t)row * g.ldo + c);
+      o[0] = __floats2half2_rn(v.x, v.y);
+      o[1] = __floats2half2_rn(v.z, v.w);
     } else {
       const int tok = g.perm[row];
+      if ((unsigned)tok >= (unsigned)g.n_tokens) {
+        record_status(g.status, kErrBounds);
+        continue;
+      }
       const float w = g.slot_w[row];
-      if (g.mode == kModeDirect) g.out[(size_t)tok * g.ldo + c] = __float2half_rn(w * v);
-      else if (g.mode == kModeSum) red_add_f16(g.out + (size_t)tok * g.ldo + c, __float2half_rn(w * v));
-      else red_add_f32(g.acc32 + (size_t)tok * g.ldo + c, w * v);
+      __half* o = g.out + (size_t)tok * g.ldo + c;
+      if (g.mode == kModeDirect) {
+        reinterpret_cast<__half2*>(o)[0] = __floats2half2_rn(w * v.x, w * v.y);
+        reinterpret_cast<__half2*>(o)[1] = __floats2half2_rn(w * v.z, w * v.w);
+      } else if (g.mode == kModeSum) {
+        red_add_f16x2(o, __floats2half2_rn(w * v.x, w * v.y));
+        red_add_f16x2(o + 2, __floats2half2_rn(w * v.z, w * v.w));
+      } else {
+        float* a32 = g.acc32 + (size_t)tok * g.ldo + c;
+        red_add_f32(a32, w * v.x);
+        red_add_f32(a32 + 1, w * v.y);
+        red_add_f32(a32 + 2, w * v.z);
+        red_add_f32(a32 + 3, w * v.w);
+      }
     }
   }
 }
@@ -221,6 +270,7 @@ cudaError_t launch_splitk_reduce1(const GemmArgs& g, int S_max, int T_res, int f
 
 cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d, cudaStream_t s,
                                   bool pdl) {
+  // four threads per four columns (d % 4 == 0; partial and the outputs 16-byte aligned)
   const size_t n = (size_t)(S_max + T_res) * d;
   return launch_k(splitk_reduce2_kernel, grid_for(n, 256), 256, 0, s, pdl, g, S_max, T_res, d);
 }
