@@ -272,7 +272,9 @@ int choose_mw2(int S_rows, int M, long long res_tiles, const TcPlan& p, int E, i
 // Decode-sized batches: weight blocks per item (mw) and K chunks per item (ks) together.
 // All work units (items x chunks) should run in one round, one per CTA; the widest mw that
 // still spreads the weights over at least half the SMs wins (measured: wider items keep more
-// bytes in flight per CTA and beat narrower ones that fill every SM); a chunk keeps at least
+// bytes in flight per CTA and beat narrower ones that fill every SM), except that a narrower
+// mw without K chunks wins over a split one that spreads the weights as widely (the same bytes
+// per CTA, and neither fp32 partial sums nor the reduction launch); a chunk keeps at least
 // two 64-wide K blocks.  mw candidates must divide every group's M and fit TMEM and three stages.
 void choose_split(long long row_tiles, int M_exp, long long res_tiles, int M_res, int nkb_min,
                   const TcPlan& p, int E, int* mw_out, int* ks_out) {
@@ -285,7 +287,9 @@ void choose_split(long long row_tiles, int M_exp, long long res_tiles, int M_res
     int ks = 1;
     while (ks * 2 <= kMaxSplit && items * ks * 2 <= p.grid && nkb_min / (ks * 2) >= 2) ks *= 2;
     const int score = (int)std::min<long long>(items * ks, p.grid / 2);
-    if (score > best) {
+    // equal spread: unsplit items win (no fp32 partial sums, no reduction launch); otherwise
+    // the widest mw
+    if (score > best || (score == best && ks == 1 && *ks_out > 1)) {
       best = score;
       *mw_out = mw;
       *ks_out = ks;

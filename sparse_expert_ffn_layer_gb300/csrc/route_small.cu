@@ -9,30 +9,44 @@
 // per-expert token capacity).
 //
 // Shape of the work.  At decode sizes the gate is latency-bound: T * E chains of d dependent
-// FMAs and a Wg read of d * E * 4 bytes.  Each CTA owns 8 experts x 32 tokens (one chain per
-// thread) and streams its Wg columns and token rows through a four-deep cp.async ring, so
-// E / 8 CTAs (16 at E = 128) pull Wg in parallel.  The last CTA to finish (a counter in the
+// FMAs and a Wg read of d * E * 4 bytes.  Each CTA owns 4 experts x 64 tokens (one chain per
+// thread) and streams its Wg columns and the batch's token rows through a four-deep cp.async
+// ring, so E / 4 CTAs (32 at E = 128) pull Wg in parallel.  The last CTA to finish (a counter in the
 // workspace, cleared by the caller before the launch and by that CTA after use) then routes
 // the whole batch: a warp per token for softmax / top-k, then the dispatch of the T * k <= 128
 // assignments by one block (per-expert counts and ranks counted directly over the assignment
 // list, no atomics).
+#include <algorithm>
+
 #include "launch.h"
 #include "topk.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRExp = 8;            // experts per CTA
-constexpr int kRTok = 32;           // tokens per CTA
+constexpr int kRExp = 4;            // experts per CTA
+constexpr int kRTok = 64;           // tokens per CTA (T <= 64: one row of CTAs)
 constexpr int kRKC = 128;           // shared-dimension chunk
 constexpr int kRStages = 4;         // cp.async ring depth
 constexpr int kRXPitch = kRKC + 8;  // halves per staged token row: the 16-byte pad spreads the
-                                    // four rows a warp reads over distinct banks
+                                    // eight rows a warp reads over distinct banks
 constexpr int kRThreads = kRExp * kRTok;
+constexpr int kRTokPerWarp = 32 / kRExp;
 constexpr size_t kRWBytes = (size_t)kRKC * kRExp * 4;
-constexpr size_t kRXBytes = (size_t)kRTok * kRXPitch * 2;
-constexpr size_t kRStageBytes = kRWBytes + kRXBytes;
-constexpr size_t kRSmem = kRStages * kRStageBytes;
+
+// Shared memory of a launch: the ring (Wg chunk and the batch's token rows per stage), and at
+// least the routing scratch the last CTA reuses it for.
+// Token rows per stage: the batch's, rounded up to whole warps (a warp's threads read the rows
+// of its eight tokens, valid or not; only valid tokens' results are stored).
+__host__ __device__ inline size_t route_stage_bytes(int nT) {
+  const int rows = (nT + kRTokPerWarp - 1) / kRTokPerWarp * kRTokPerWarp;
+  return kRWBytes + (size_t)rows * kRXPitch * 2;
+}
+inline size_t route_smem_bytes(int nT, int E) {
+  const size_t ring = kRStages * route_stage_bytes(nT);
+  const size_t scratch = (size_t)(256 + 2 * E + kRThreads / 32) * 4;
+  return ring > scratch ? ring : scratch;
+}
 
 struct RouteArgs {
   const __half* x;       // [T, d]
@@ -74,17 +88,16 @@ __global__ void __launch_bounds__(kRThreads) gate_route_small_kernel(const Route
   const int e0 = blockIdx.x * kRExp, t0 = blockIdx.y * kRTok;
   const int nT = min(kRTok, a.T - t0);
   const int nch = a.d / kRKC;
-  // a warp holds tokens 4w .. 4w+3: warps past the batch's last token only help load
-  const bool computes = (tt & ~3) < nT;
+  const size_t stage_bytes = route_stage_bytes(min(kRTok, a.T));
+  // a warp holds tokens 8w .. 8w+7: warps past the batch's last token only help load
+  const bool computes = (tt & ~(kRTokPerWarp - 1)) < nT;
 
   auto issue = [&](int c) {
-    uint8_t* base = sm + (size_t)(c % kRStages) * kRStageBytes;
+    uint8_t* base = sm + (size_t)(c % kRStages) * stage_bytes;
     const int i0 = c * kRKC;
-    {   // Wg rows i0 .. i0+127, experts e0 .. e0+7: one 16-byte piece per thread
-      const int row = threadIdx.x >> 1, part = threadIdx.x & 1;
-      cp_async16(base + row * (kRExp * 4) + part * 16,
-                 a.Wg + (size_t)(i0 + row) * a.E + e0 + part * 4);
-    }
+    // Wg rows i0 .. i0+127, experts e0 .. e0+3: one 16-byte piece per row
+    for (int row = threadIdx.x; row < kRKC; row += kRThreads)
+      cp_async16(base + row * (kRExp * 4), a.Wg + (size_t)(i0 + row) * a.E + e0);
     uint8_t* xb = base + kRWBytes;     // the valid token rows, 16 pieces each
     for (int q = threadIdx.x; q < nT * (kRKC / 8); q += kRThreads) {
       const int r = q / (kRKC / 8), col = (q % (kRKC / 8)) * 8;
@@ -103,7 +116,7 @@ __global__ void __launch_bounds__(kRThreads) gate_route_small_kernel(const Route
     cp_async_commit();
     cp_async_wait<kRStages - 1>();
     __syncthreads();
-    const uint8_t* base = sm + (size_t)(c % kRStages) * kRStageBytes;
+    const uint8_t* base = sm + (size_t)(c % kRStages) * stage_bytes;
     const float* ws = reinterpret_cast<const float*>(base) + ee;
     const __half* xs = reinterpret_cast<const __half*>(base + kRWBytes) + tt * kRXPitch;
     if (computes) {
@@ -217,7 +230,7 @@ __global__ void __launch_bounds__(kRThreads) gate_route_small_kernel(const Route
 }  // namespace
 
 bool gate_route_small_ok(int T, int d, int E, const void* x, const void* Wg) {
-  return T >= 1 && T <= 64 && d % kRKC == 0 && E % kRExp == 0 && E <= 1024 &&
+  return T >= 1 && T <= kRTok && d % kRKC == 0 && E % kRExp == 0 && E <= 1024 &&
          (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (reinterpret_cast<uintptr_t>(Wg) & 15) == 0;
 }
 
@@ -231,7 +244,8 @@ cudaError_t launch_gate_route_small(const __half* x, const float* Wg, int T, int
   RouteArgs a{x, Wg, T, d, E, k, C, logits, topk_idx, topk_w, counts_raw, kept, offsets, perm,
               slot_of, slot_w, counter};
   dim3 grid(E / kRExp, (T + kRTok - 1) / kRTok);
-  return launch_k(gate_route_small_kernel, grid, kRThreads, kRSmem, s, false, a);
+  return launch_k(gate_route_small_kernel, grid, kRThreads, route_smem_bytes(std::min(T, kRTok), E),
+                  s, false, a);
 }
 
 }  // namespace moe
