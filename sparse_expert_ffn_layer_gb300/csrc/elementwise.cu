@@ -181,11 +181,12 @@ __global__ void splitk_reduce1_kernel(const GemmArgs g, int S_max, int T_res, in
   }
 }
 
-// Split-K reduction of the second GEMM, then the combine.  Four threads (a quad of lanes)
-// share four adjacent columns of one partial row: thread p sums chunks p, p + 4, p + 8, ... in
-// ascending order with 16-byte loads, all independent, so many are in flight at once; the quad
-// then adds (s0 + s1) + (s2 + s3) (each pair added in the same order by both lanes that form
-// it), so every run gives the same bits.
+// Split-K reduction of the second GEMM, then the combine.  At decode sizes its time is the
+// latency of its loads: four threads (a quad of lanes) share four adjacent columns of one
+// partial row, thread p sums chunks p, p + 4, p + 8, ... in ascending order with 16-byte loads
+// (all independent, so they are in flight together, beside the slot's token and gate weight),
+// and the quad then adds (s0 + s1) + (s2 + s3) (each pair added in the same order by both lanes
+// that form it), so every run gives the same bits.
 __global__ void splitk_reduce2_kernel(const GemmArgs g, int S_max, int T_res, int d) {
   pdl_wait();
   pdl_trigger();
@@ -204,6 +205,14 @@ __global__ void splitk_reduce2_kernel(const GemmArgs g, int S_max, int T_res, in
     const int row = res ? prow - S_max : prow;
     const bool live = q < n && (res || row < S);
     const int nks = g.ksplit;
+    // the slot's token and gate weight first, so that their loads overlap the partial sums'
+    int tok = 0;
+    float w = 1.0f;
+    const bool scatter = live && !res && g.mode != kModeExpertOut;
+    if (scatter) {
+      tok = g.perm[row];
+      w = g.slot_w[row];
+    }
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) {
       const float* base = g.partial + (size_t)prow * g.part_cols + c;
@@ -235,12 +244,10 @@ __global__ void splitk_reduce2_kernel(const GemmArgs g, int S_max, int T_res, in
       o[0] = __floats2half2_rn(v.x, v.y);
       o[1] = __floats2half2_rn(v.z, v.w);
     } else {
-      const int tok = g.perm[row];
       if ((unsigned)tok >= (unsigned)g.n_tokens) {
         record_status(g.status, kErrBounds);
         continue;
       }
-      const float w = g.slot_w[row];
       __half* o = g.out + (size_t)tok * g.ldo + c;
       if (g.mode == kModeDirect) {
         reinterpret_cast<__half2*>(o)[0] = __floats2half2_rn(w * v.x, w * v.y);
@@ -270,7 +277,6 @@ cudaError_t launch_splitk_reduce1(const GemmArgs& g, int S_max, int T_res, int f
 
 cudaError_t launch_splitk_reduce2(const GemmArgs& g, int S_max, int T_res, int d, cudaStream_t s,
                                   bool pdl) {
-  // four threads per four columns (d % 4 == 0; partial and the outputs 16-byte aligned)
   const size_t n = (size_t)(S_max + T_res) * d;
   return launch_k(splitk_reduce2_kernel, grid_for(n, 256), 256, 0, s, pdl, g, S_max, T_res, d);
 }

@@ -373,13 +373,17 @@ __global__ void __launch_bounds__(Roles<kSplit>::kThreads, 1)
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = smem_u32(smem + (size_t)stage * L.stage_bytes);
-          const uint32_t b0 = a0 + L.b_off;
+          // descriptors of the stage's first A block and B rows; the others differ only in
+          // the start address (in 16-byte units, bits 0..13, which shared-memory addresses
+          // below 256 KB never carry out of)
+          const uint64_t ad0 = smem_desc(a0, a.a_lbo, a.a_sbo, 2);
+          const uint64_t bd0 = smem_desc(a0 + L.b_off, 16, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
+            const uint64_t bd = bd0 + (uint64_t)(kk * 32 / 16);
 #pragma unroll
             for (int h = 0; h < mw; ++h) {             // same token rows, mw weight blocks
-              const uint64_t ad = smem_desc(a0 + h * kABytes + kk * 2048, a.a_lbo, a.a_sbo, 2);
+              const uint64_t ad = ad0 + (uint64_t)((h * kABytes + kk * 2048) / 16);
               tc_mma_f16(d_tmem[h], ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
             }
           }
