@@ -79,7 +79,7 @@ struct L2Load {
   __device__ __forceinline__ float operator()(const float* p) const { return __ldcg(p); }
 };
 
-// Needs f16 tokens, d % 128 == 0, E % 8 == 0, 16-byte aligned x and Wg, T <= 64.
+// Needs f16 tokens, d % 128 == 0, E % 4 == 0, 16-byte aligned x and Wg, T <= 64.
 __global__ void __launch_bounds__(kRThreads) gate_route_small_kernel(const RouteArgs a) {
   pdl_trigger();
   extern __shared__ __align__(16) uint8_t sm[];
